@@ -1,0 +1,69 @@
+// Host-side declarations shared by the kernel files and the C-ABI layer (api.cu).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/moe_fp8.h"
+
+namespace moe {
+
+// Multiprocessor count of the current device (cached per device).
+int num_sms();
+
+// MOE_OK if the last launch succeeded, else MOE_ERR_CUDA (and clears the error).
+int check_launch();
+
+int launch_quant_1x128(const uint16_t* x, int rows, int cols, int ldx, uint8_t* q,
+                       float* scale, cudaStream_t stream);
+int launch_quant_128x128(const float* w, int rows, int cols, uint8_t* q, float* scale,
+                         cudaStream_t stream);
+
+int launch_route(const float* scores, int aff, const float* bias, int T, int E, int n_groups,
+                 int topk_groups, int group_topn, int K, float route_scale, int32_t* idx,
+                 float* gate, cudaStream_t stream);
+
+size_t permute_ws_bytes(int T, int K, int E);
+int launch_permute(const int32_t* idx, int T, int K, int E, int include_shared,
+                   int32_t* counts, int32_t* offsets, int32_t* row_token, int32_t* row_of,
+                   int32_t* status, void* ws, cudaStream_t stream);
+
+int launch_combine(const uint16_t* y_rows, int n_rows, const int32_t* row_of,
+                   const float* gate, int T, int K, int d, int shared_row_base, uint16_t* y,
+                   int32_t* status, cudaStream_t stream);
+
+int launch_bias_update(float* bias, const int32_t* counts, int E, int T, int K, float gamma,
+                       cudaStream_t stream);
+
+// Copy rows: dst[r] = src[rows[r]] for r < min(n_rows, *row_limit) (row_limit on the
+// device; NULL = n_rows), for an FP8 matrix of `cols` columns and its 1x128 scales
+// ([cols/128][src_rows] -> [cols/128][n_rows]).
+int launch_gather_rows_fp8(const uint8_t* src, const float* src_scale, int src_rows,
+                           const int32_t* rows, const int32_t* row_limit, int n_rows, int cols,
+                           uint8_t* dst, float* dst_scale, int32_t* status,
+                           cudaStream_t stream);
+
+// Grouped block-scaled GEMM (tcgen05).  Epilogue kinds:
+enum GemmEpilogue { kEpiBF16 = 0, kEpiSwiGLU = 1 };
+struct GemmArgs {
+  const uint8_t* A;      // [M][K] rows already in segment order
+  const float* sA;       // [K/128][M]
+  const uint8_t* B;      // [G][N][K]
+  const float* sB;       // [G][N/128][K/128]
+  const int32_t* seg;    // [G+1] device
+  int G, M, N, K;
+  uint16_t* C;           // kEpiBF16: [M][ldc] BF16
+  int ldc;
+  uint8_t* hq;           // kEpiSwiGLU: [M][N/2] E4M3
+  float* sh;             // kEpiSwiGLU: [N/256][M]
+  int32_t* status;
+};
+int launch_fp8_gemm(const GemmArgs& a, GemmEpilogue epi, cudaStream_t stream);
+
+int launch_router_logits(const uint16_t* x, int T, int d, const uint16_t* w_hilo, int E,
+                         float* z, void* ws, cudaStream_t stream);
+size_t router_logits_ws_bytes(int T, int d, int E);
+int launch_router_split(const float* w, long long n, uint16_t* w_hilo, cudaStream_t stream);
+
+}  // namespace moe

@@ -1,0 +1,152 @@
+// Dispatch metadata: group the (token, slot) pairs into expert-contiguous segments
+// ("DeepSeek-V3" book, ch. 15 "What dispatch must do" -- rows grouped by expert, with
+// metadata naming the source token so combine can restore it; ch. 7 "Batches change
+// what is active"; no token dropping, "DeepSeek-V3" summary, core idea 1).
+//
+// A stable counting sort keyed by expert, in three passes over token chunks:
+//   count    per-chunk histograms
+//   scan     per-expert totals, exclusive scan -> segment offsets, per-chunk bases
+//   scatter  thread e walks the chunk's pairs in (token, slot) order and hands out rows
+// Every step is integer work in a fixed order, so the result is deterministic and equal
+// to a stable sort whatever the launch timing.
+#include "common.cuh"
+#include "launch.h"
+
+namespace moe {
+
+namespace {
+constexpr int kChunkTokens = 128;
+constexpr int kPermThreads = 256;
+constexpr int kScanThreads = 1024;
+
+int n_chunks(int T) { return (T + kChunkTokens - 1) / kChunkTokens; }
+}  // namespace
+
+size_t permute_ws_bytes(int T, int K, int E) {
+  (void)K;
+  return static_cast<size_t>(n_chunks(T)) * E * sizeof(int32_t);
+}
+
+__global__ void __launch_bounds__(kPermThreads) permute_count_kernel(
+    const int32_t* __restrict__ idx, int T, int K, int E, int32_t* __restrict__ chunk_counts,
+    int32_t* status) {
+  extern __shared__ int32_t hist[];
+  const int c = blockIdx.x;
+  const int t0 = c * kChunkTokens;
+  const int np = min(kChunkTokens, T - t0) * K;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  const int32_t* src = idx + static_cast<long long>(t0) * K;
+  for (int p = threadIdx.x; p < np; p += blockDim.x) {
+    const int e = src[p];
+    if (e < 0 || e >= E) set_status(status, MOE_ERR_DEVICE_DATA);
+    else atomicAdd(&hist[e], 1);              // integer counts: order does not matter
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    chunk_counts[static_cast<long long>(c) * E + e] = hist[e];
+}
+
+// Block-wide exclusive scan of one value per thread (kScanThreads threads).
+__device__ int block_exclusive_scan(int v, int* warp_sums) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = (lane < kScanThreads / 32) ? warp_sums[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xFFFFFFFFu, wi, off);
+      if (lane >= off) wi += o;
+    }
+    warp_sums[lane] = wi - w;                  // exclusive prefix of warp totals
+  }
+  __syncthreads();
+  return warp_sums[warp] + incl - v;
+}
+
+__global__ void __launch_bounds__(kScanThreads) permute_scan_kernel(
+    int32_t* __restrict__ chunk_counts /* in: counts, out: bases */, int nchunks, int T, int K,
+    int E, int include_shared, int32_t* __restrict__ counts, int32_t* __restrict__ offsets) {
+  __shared__ int warp_sums[32];
+  const int e = threadIdx.x;                   // E <= kScanThreads
+  int total = 0;
+  if (e < E) {
+    for (int c = 0; c < nchunks; ++c) {
+      int32_t* p = chunk_counts + static_cast<long long>(c) * E + e;
+      const int n = *p;
+      *p = total;                              // running base within the expert
+      total += n;
+    }
+  }
+  const int off = block_exclusive_scan(e < E ? total : 0, warp_sums);
+  if (e < E) {
+    counts[e] = total;
+    offsets[e] = off;
+    for (int c = 0; c < nchunks; ++c) chunk_counts[static_cast<long long>(c) * E + e] += off;
+  }
+  if (e == 0) {
+    offsets[E] = T * K;
+    offsets[E + 1] = T * K + (include_shared ? T : 0);
+  }
+}
+
+__global__ void __launch_bounds__(kPermThreads) permute_scatter_kernel(
+    const int32_t* __restrict__ idx, int T, int K, int E, int include_shared,
+    const int32_t* __restrict__ chunk_base, int32_t* __restrict__ row_token,
+    int32_t* __restrict__ row_of) {
+  extern __shared__ int32_t pairs[];
+  const int c = blockIdx.x;
+  const int t0 = c * kChunkTokens;
+  const int nt = min(kChunkTokens, T - t0);
+  const int np = nt * K;
+  const int32_t* src = idx + static_cast<long long>(t0) * K;
+  for (int p = threadIdx.x; p < np; p += blockDim.x) pairs[p] = src[p];
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int row = chunk_base[static_cast<long long>(c) * E + e];
+    for (int p = 0; p < np; ++p) {             // (token, slot) order: stable
+      if (pairs[p] == e) {
+        const int t = t0 + p / K;
+        row_of[static_cast<long long>(t0) * K + p] = row;
+        row_token[row] = t;
+        ++row;
+      }
+    }
+  }
+  if (include_shared) {
+    const long long base = static_cast<long long>(T) * K;
+    for (int i = threadIdx.x; i < nt; i += blockDim.x) row_token[base + t0 + i] = t0 + i;
+  }
+}
+
+int launch_permute(const int32_t* idx, int T, int K, int E, int include_shared,
+                   int32_t* counts, int32_t* offsets, int32_t* row_token, int32_t* row_of,
+                   int32_t* status, void* ws, cudaStream_t stream) {
+  const int nc = n_chunks(T);
+  int32_t* chunk = static_cast<int32_t*>(ws);
+  if (nc > 0) {
+    permute_count_kernel<<<nc, kPermThreads, E * sizeof(int32_t), stream>>>(idx, T, K, E, chunk,
+                                                                            status);
+    if (check_launch() != MOE_OK) return MOE_ERR_CUDA;
+  }
+  permute_scan_kernel<<<1, kScanThreads, 0, stream>>>(chunk, nc, T, K, E, include_shared, counts,
+                                                       offsets);
+  if (check_launch() != MOE_OK) return MOE_ERR_CUDA;
+  if (nc > 0) {
+    const size_t smem = static_cast<size_t>(kChunkTokens) * K * sizeof(int32_t);
+    permute_scatter_kernel<<<nc, kPermThreads, smem, stream>>>(idx, T, K, E, include_shared,
+                                                                chunk, row_token, row_of);
+    if (check_launch() != MOE_OK) return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+}  // namespace moe

@@ -1,0 +1,117 @@
+// Online FP8 quantisation: BF16 activations in 1x128 tiles (fp8_quant_1x128) and FP32
+// weights in 128x128 blocks (fp8_quant_128x128, setup only).
+//
+// The scale of a group is its max-abs divided by the E4M3 maximum 448, so the largest
+// element lands on +-448 ("DeepSeek-V3" summary, core idea 6(a) fine-grained tiles and
+// 6(d) online scaling; "DeepSeek-V3" book, ch. 16 "V3's grouping", "Online scales",
+// "Scaling a group").  Quantised values are E4M3 round-to-nearest-even with saturation.
+#include "common.cuh"
+#include "launch.h"
+
+namespace moe {
+
+// Half a warp per 1x128 tile: 16 lanes x 8 BF16 values.  Tiles are numbered with the
+// column block fastest so a warp reads 512 contiguous bytes of one row.
+__global__ void __launch_bounds__(256) quant_1x128_kernel(const uint16_t* __restrict__ x,
+                                                           int rows, int ncb, int ldx,
+                                                           uint8_t* __restrict__ q,
+                                                           float* __restrict__ scale,
+                                                           long long ntiles) {
+  const int lane = threadIdx.x & 31;
+  const int half = lane >> 4;
+  const int hl = lane & 15;
+  const long long warp = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  const long long cols = static_cast<long long>(ncb) * 128;
+  for (long long p = warp; 2 * p < ntiles; p += nwarps) {
+    const long long t = 2 * p + half;
+    const bool valid = t < ntiles;
+    const long long r = valid ? t / ncb : 0;
+    const int cb = valid ? static_cast<int>(t % ncb) : 0;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (valid)
+      v = __ldcs(reinterpret_cast<const uint4*>(x + r * ldx + cb * 128 + hl * 8));
+    float f[8];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f[2 * i] = __uint_as_float(w[i] << 16);
+      f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1)
+      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+    const float s = e4m3_scale_from_amax(amax);
+    uint32_t out[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const uint32_t a = f32x2_to_e4m3x2(__fdiv_rn(f[4 * i], s), __fdiv_rn(f[4 * i + 1], s));
+      const uint32_t b = f32x2_to_e4m3x2(__fdiv_rn(f[4 * i + 2], s), __fdiv_rn(f[4 * i + 3], s));
+      out[i] = a | (b << 16);
+    }
+    if (valid) {
+      *reinterpret_cast<uint2*>(q + r * cols + cb * 128 + hl * 8) = make_uint2(out[0], out[1]);
+      if (hl == 0) scale[static_cast<long long>(cb) * rows + r] = s;
+    }
+  }
+}
+
+// One block per 128x128 weight block; thread t covers row t/2, 64 columns.
+__global__ void __launch_bounds__(256) quant_128x128_kernel(const float* __restrict__ w,
+                                                             int rows, int cols,
+                                                             uint8_t* __restrict__ q,
+                                                             float* __restrict__ scale) {
+  const int rb = blockIdx.y, cb = blockIdx.x;
+  const int r = rb * 128 + (threadIdx.x >> 1);
+  const int c0 = cb * 128 + (threadIdx.x & 1) * 64;
+  const float* src = w + static_cast<long long>(r) * cols + c0;
+  float amax = 0.0f;
+  for (int i = 0; i < 64; i += 4) {
+    const float4 v = *reinterpret_cast<const float4*>(src + i);
+    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1)
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+  __shared__ float wmax[8];
+  if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = wmax[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) amax = fmaxf(amax, wmax[i]);
+  const float s = e4m3_scale_from_amax(amax);
+  uint8_t* dst = q + static_cast<long long>(r) * cols + c0;
+  for (int i = 0; i < 64; i += 4) {
+    const float4 v = *reinterpret_cast<const float4*>(src + i);
+    const uint32_t a = f32x2_to_e4m3x2(__fdiv_rn(v.x, s), __fdiv_rn(v.y, s));
+    const uint32_t b = f32x2_to_e4m3x2(__fdiv_rn(v.z, s), __fdiv_rn(v.w, s));
+    *reinterpret_cast<uint32_t*>(dst + i) = a | (b << 16);
+  }
+  if (threadIdx.x == 0) scale[static_cast<long long>(rb) * (cols / 128) + cb] = s;
+}
+
+int launch_quant_1x128(const uint16_t* x, int rows, int cols, int ldx, uint8_t* q,
+                       float* scale, cudaStream_t stream) {
+  const long long ntiles = static_cast<long long>(rows) * (cols / 128);
+  if (ntiles == 0) return MOE_OK;
+  const long long pairs = (ntiles + 1) / 2;
+  long long blocks = (pairs + 7) / 8;                 // 8 warps per block
+  const long long cap = static_cast<long long>(num_sms()) * 16;
+  if (blocks > cap) blocks = cap;
+  quant_1x128_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(x, rows, cols / 128, ldx,
+                                                                        q, scale, ntiles);
+  return check_launch();
+}
+
+int launch_quant_128x128(const float* w, int rows, int cols, uint8_t* q, float* scale,
+                         cudaStream_t stream) {
+  if (rows == 0 || cols == 0) return MOE_OK;
+  dim3 grid(cols / 128, rows / 128);
+  quant_128x128_kernel<<<grid, 256, 0, stream>>>(w, rows, cols, q, scale);
+  return check_launch();
+}
+
+}  // namespace moe

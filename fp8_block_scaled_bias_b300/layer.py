@@ -1,0 +1,128 @@
+"""One DeepSeek-V3 MoE FFN layer forward, assembled from the C-ABI calls.
+
+The order is the one the pages give for a MoE layer ("DeepSeek-V3" book, ch. 7 and
+ch. 15; "DeepSeek-V3" summary, core ideas 1, 2 and 6): router logits kept above FP8,
+sigmoid affinities with the selection-only bias and the group limit, normalised gates,
+FP8 quantisation of the activations before dispatch, grouping of rows by expert,
+SwiGLU experts as block-scaled FP8 grouped GEMMs (routed experts and the shared expert
+as one more segment), and the gate-weighted BF16 combine.  The layer output excludes
+the residual; ``forward(..., residual=True)`` adds x afterwards.
+
+Weights are prepared once (not timed): expert matrices are quantised 128x128 on the
+GPU and the gate/up matrices are interleaved in 128-row blocks so one 256-column GEMM
+tile holds matching gate and up columns.
+"""
+
+from dataclasses import dataclass
+
+import torch
+
+from . import ops
+
+
+@dataclass
+class MoEWeights:
+    centroids: torch.Tensor   # FP32 [E, d]
+    w_hilo: torch.Tensor      # BF16 [2, E, d]
+    bias: torch.Tensor        # FP32 [E]
+    w13: torch.Tensor         # E4M3 [E+1, 2f, d], gate/up interleaved in 128-row blocks
+    s13: torch.Tensor         # FP32 [E+1, 2f/128, d/128]
+    w2: torch.Tensor          # E4M3 [E+1, d, f]
+    s2: torch.Tensor          # FP32 [E+1, d/128, f/128]
+
+
+def interleave_gate_up(q1, s1, q3, s3):
+    """Gate [f, d] and up [f, d] codes/scales -> [2f, d] with alternating 128-row blocks."""
+    f, d = q1.shape
+    w13 = torch.stack([q1.view(f // 128, 128, d), q3.view(f // 128, 128, d)], dim=1)
+    s13 = torch.stack([s1, s3], dim=1)
+    return w13.reshape(2 * f, d), s13.reshape(2 * f // 128, d // 128)
+
+
+def quantise_expert(w1, w3, w2):
+    """FP32 (w1 [f,d], w3 [f,d], w2 [d,f]) on the GPU -> (w13, s13, w2q, s2) via the library."""
+    q1, s1 = ops.quant_128x128(w1.contiguous())
+    q3, s3 = ops.quant_128x128(w3.contiguous())
+    q2, s2 = ops.quant_128x128(w2.contiguous())
+    w13, s13 = interleave_gate_up(q1, s1, q3, s3)
+    return w13, s13, q2, s2
+
+
+def make_weights(cfg, device="cuda", base_seed=0, expert_fn=None):
+    """Seeded synthetic weights for ``cfg`` (a workloads.MoEConfig), quantised on the GPU.
+
+    ``expert_fn(e)`` may override the FP32 expert generator (returns w1, w3, w2)."""
+    import workloads
+    dev = torch.device(device)
+    cen = workloads.gen_centroids(cfg, base_seed).to(dev)
+    bias = workloads.gen_bias(cfg, base_seed).to(dev)
+    E, d, f = cfg.E, cfg.d, cfg.f
+    w13 = torch.empty(E + 1, 2 * f, d, dtype=torch.uint8, device=dev)
+    s13 = torch.empty(E + 1, 2 * f // 128, d // 128, dtype=torch.float32, device=dev)
+    w2 = torch.empty(E + 1, d, f, dtype=torch.uint8, device=dev)
+    s2 = torch.empty(E + 1, d // 128, f // 128, dtype=torch.float32, device=dev)
+    for e in range(E + 1):
+        if expert_fn is None:
+            w = workloads.gen_expert_f32(cfg, e, device=dev, base_seed=base_seed)
+        else:
+            w = tuple(t.to(dev) for t in expert_fn(e))
+        w13[e], s13[e], w2[e], s2[e] = quantise_expert(*w)
+        del w
+    return MoEWeights(cen, ops.router_split_bf16(cen), bias, w13, s13, w2, s2)
+
+
+class MoELayer:
+    """Buffers and the sequence of library calls for one layer forward."""
+
+    def __init__(self, cfg, weights, T=None):
+        self.cfg = cfg
+        self.w = weights
+        self.T = cfg.T if T is None else T
+        T, E, K, d, f = self.T, cfg.E, cfg.K, cfg.d, cfg.f
+        dev = weights.w13.device
+        self.rows = T * K + T
+        emp = lambda *s, dt=torch.float32: torch.empty(*s, dtype=dt, device=dev)
+        self.z = emp(T, E)
+        self.idx = emp(T, K, dt=torch.int32)
+        self.gate = emp(T, K)
+        self.counts = emp(E, dt=torch.int32)
+        self.offsets = emp(E + 2, dt=torch.int32)
+        self.row_token = emp(self.rows, dt=torch.int32)
+        self.row_of = emp(T, K, dt=torch.int32)
+        self.xq = emp(T, d, dt=torch.uint8)
+        self.sx = emp(d // 128, T)
+        self.hq = emp(self.rows, f, dt=torch.uint8)
+        self.sh = emp(f // 128, self.rows)
+        self.y_rows = emp(self.rows, d, dt=torch.bfloat16)
+        self.y = emp(T, d, dt=torch.bfloat16)
+        self.status = ops.new_status(dev)
+        self.launches_per_forward = 10     # logits, route, permute x3, quant, gather, GEMM x2, combine
+
+    def forward(self, x, logits=None, residual=False):
+        """x BF16 [T, d] on the device -> y BF16 [T, d] (the layer's own buffer)."""
+        cfg, w = self.cfg, self.w
+        if logits is None:
+            ops.router_logits(x, w.w_hilo, out=self.z)
+            z = self.z
+        else:
+            z = logits
+        ops.route(z, w.bias, cfg.n_groups, cfg.topk_groups, cfg.K, out=(self.idx, self.gate))
+        ops.permute(self.idx, cfg.E, True, self.status,
+                    out=(self.counts, self.offsets, self.row_token, self.row_of))
+        ops.quant_1x128(x, out=(self.xq, self.sx))
+        ops.swiglu_fwd(self.xq, self.sx, self.row_token, self.offsets, self.rows, w.w13, w.s13,
+                       w.w2, w.s2, self.status, out=(self.hq, self.sh, self.y_rows))
+        ops.combine(self.y_rows, self.row_of, self.gate, self.T * cfg.K, self.status, out=self.y)
+        if residual:
+            return self.y + x
+        return self.y
+
+    def bias_update(self, gamma):
+        """Aux-loss-free bias step from this forward's expert loads (in place)."""
+        ops.bias_update(self.w.bias, self.counts, self.T, self.cfg.K, gamma)
+
+    def check_status(self):
+        st = ops.status_value(self.status)
+        if st != 0:
+            from ._lib import STATUS
+            raise RuntimeError(f"device status {STATUS.get(st, st)}")

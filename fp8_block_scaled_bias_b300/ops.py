@@ -1,0 +1,222 @@
+"""PyTorch-facing wrappers of the C-ABI entry points.
+
+Each wrapper checks dtypes, shapes, device and contiguity, allocates its outputs with
+torch (the library itself never allocates), and passes raw device pointers plus the
+current CUDA stream.  No arithmetic of the method happens here.
+"""
+
+import torch
+
+from ._lib import call, load
+
+_U8, _F32, _I32, _BF16 = torch.uint8, torch.float32, torch.int32, torch.bfloat16
+
+
+def _ptr(t):
+    return t.data_ptr() if t is not None else None
+
+
+def _stream():
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _check(t, dtype, name, ndim=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {t.dim()}")
+
+
+class Workspace:
+    """A growing per-device scratch buffer handed to calls that need workspace."""
+
+    def __init__(self):
+        self._buf = {}
+
+    def get(self, nbytes, device):
+        if nbytes <= 0:
+            return None, 0
+        key = torch.device(device).index or 0
+        b = self._buf.get(key)
+        if b is None or b.numel() < nbytes:
+            b = torch.empty(nbytes, dtype=_U8, device=device)
+            self._buf[key] = b
+        return b.data_ptr(), b.numel()
+
+
+WS = Workspace()
+
+
+def new_status(device):
+    """int32 device status word (0 = OK) for calls that report device-side errors."""
+    return torch.zeros(1, dtype=_I32, device=device)
+
+
+def status_value(status):
+    return int(status.item())
+
+
+# ---- router -----------------------------------------------------------------------------
+
+def router_split_bf16(w):
+    """FP32 centroids [E, d] -> BF16 planes [2, E, d] = (bf16(w), bf16(w - hi))."""
+    _check(w, _F32, "w", 2)
+    out = torch.empty((2,) + tuple(w.shape), dtype=_BF16, device=w.device)
+    call("moe_router_split_bf16", _ptr(w), w.numel(), _ptr(out), _stream())
+    return out
+
+
+def router_logits(x, w_hilo, out=None):
+    """z [T, E] FP32 = x [T, d] (BF16) . (hi + lo)^T."""
+    _check(x, _BF16, "x", 2)
+    _check(w_hilo, _BF16, "w_hilo", 3)
+    T, d = x.shape
+    E = w_hilo.shape[1]
+    if w_hilo.shape != (2, E, d):
+        raise ValueError("w_hilo must be [2, E, d]")
+    z = out if out is not None else torch.empty(T, E, dtype=_F32, device=x.device)
+    lib = load()
+    ws, wsb = WS.get(lib.moe_router_logits_ws_bytes(T, d, E), x.device)
+    call("moe_router_logits", _ptr(x), T, d, _ptr(w_hilo), E, _ptr(z), ws, wsb, _stream())
+    return z
+
+
+def route(scores, bias, n_groups, topk_groups, K, group_topn=None, route_scale=1.0,
+          affinities=False, out=None):
+    """(idx int32 [T, K], gate FP32 [T, K]) from logits (or affinities) [T, E]."""
+    _check(scores, _F32, "scores", 2)
+    _check(bias, _F32, "bias", 1)
+    T, E = scores.shape
+    if group_topn is None:
+        group_topn = K // topk_groups
+    if out is None:
+        idx = torch.empty(T, K, dtype=_I32, device=scores.device)
+        gate = torch.empty(T, K, dtype=_F32, device=scores.device)
+    else:
+        idx, gate = out
+    call("moe_route", _ptr(scores), int(bool(affinities)), _ptr(bias), T, E, n_groups,
+         topk_groups, group_topn, K, float(route_scale), _ptr(idx), _ptr(gate), _stream())
+    return idx, gate
+
+
+def bias_update(bias, counts, T, K, gamma):
+    """In place: bias += gamma * sign(T*K/E - counts)."""
+    _check(bias, _F32, "bias", 1)
+    _check(counts, _I32, "counts", 1)
+    call("moe_bias_update", _ptr(bias), _ptr(counts), bias.numel(), T, K, float(gamma), _stream())
+    return bias
+
+
+# ---- dispatch ---------------------------------------------------------------------------
+
+def permute(idx, E, include_shared=True, status=None, out=None):
+    """(counts [E], offsets [E+2], row_token [rows], row_of [T, K]) for idx [T, K]."""
+    _check(idx, _I32, "idx", 2)
+    T, K = idx.shape
+    dev = idx.device
+    rows = T * K + (T if include_shared else 0)
+    if out is None:
+        counts = torch.empty(E, dtype=_I32, device=dev)
+        offsets = torch.empty(E + 2, dtype=_I32, device=dev)
+        row_token = torch.empty(rows, dtype=_I32, device=dev)
+        row_of = torch.empty(T, K, dtype=_I32, device=dev)
+    else:
+        counts, offsets, row_token, row_of = out
+    lib = load()
+    ws, wsb = WS.get(lib.moe_permute_ws_bytes(T, K, E), dev)
+    call("moe_permute", _ptr(idx), T, K, E, int(bool(include_shared)), _ptr(counts),
+         _ptr(offsets), _ptr(row_token), _ptr(row_of), _ptr(status), ws, wsb, _stream())
+    return counts, offsets, row_token, row_of
+
+
+# ---- quantisation -----------------------------------------------------------------------
+
+def quant_1x128(x, out=None):
+    """BF16 [rows, cols] -> (E4M3 codes uint8 [rows, cols], scales FP32 [cols/128, rows])."""
+    _check(x, _BF16, "x", 2)
+    rows, cols = x.shape
+    if out is None:
+        q = torch.empty(rows, cols, dtype=_U8, device=x.device)
+        s = torch.empty(cols // 128, rows, dtype=_F32, device=x.device)
+    else:
+        q, s = out
+    call("fp8_quant_1x128", _ptr(x), rows, cols, cols, _ptr(q), _ptr(s), _stream())
+    return q, s
+
+
+def quant_128x128(w):
+    """FP32 [rows, cols] -> (E4M3 codes uint8, scales FP32 [rows/128, cols/128])."""
+    _check(w, _F32, "w", 2)
+    rows, cols = w.shape
+    q = torch.empty(rows, cols, dtype=_U8, device=w.device)
+    s = torch.empty(rows // 128, cols // 128, dtype=_F32, device=w.device)
+    call("fp8_quant_128x128", _ptr(w), rows, cols, _ptr(q), _ptr(s), _stream())
+    return q, s
+
+
+# ---- GEMM and experts -------------------------------------------------------------------
+
+def grouped_gemm(A, sA, B, sB, seg_offsets, M, a_rows=None, status=None, out=None):
+    """BF16 C [M, N] = block-scaled A . B_g^T per segment (see include/moe_fp8.h).
+
+    A uint8 [M_a, K], sA FP32 [K/128, M_a], B uint8 [G, N, K], sB FP32 [G, N/128, K/128],
+    seg_offsets int32 [G+1], a_rows int32 [M] or None.
+    """
+    _check(A, _U8, "A", 2)
+    _check(sA, _F32, "sA", 2)
+    _check(B, _U8, "B", 3)
+    _check(sB, _F32, "sB", 3)
+    _check(seg_offsets, _I32, "seg_offsets", 1)
+    G, N, K = B.shape
+    if a_rows is not None:
+        _check(a_rows, _I32, "a_rows", 1)
+    C = out if out is not None else torch.empty(M, N, dtype=_BF16, device=A.device)
+    lib = load()
+    ws, wsb = WS.get(lib.fp8_grouped_gemm_ws_bytes(M, K, int(a_rows is not None)), A.device)
+    call("fp8_blockscaled_grouped_gemm", _ptr(A), _ptr(sA), A.shape[0], _ptr(a_rows), _ptr(B),
+         _ptr(sB), _ptr(seg_offsets), G, M, N, K, _ptr(C), C.stride(0), _ptr(status), ws, wsb,
+         _stream())
+    return C
+
+
+def swiglu_fwd(xq, sx, row_token, offsets, rows, w13, s13, w2, s2, status=None, out=None):
+    """SwiGLU experts over expert segments: returns (hq, sh, y_rows)."""
+    for t, dt, n in ((xq, _U8, "xq"), (sx, _F32, "sx"), (row_token, _I32, "row_token"),
+                     (offsets, _I32, "offsets"), (w13, _U8, "w13"), (s13, _F32, "s13"),
+                     (w2, _U8, "w2"), (s2, _F32, "s2")):
+        _check(t, dt, n)
+    T, d = xq.shape
+    S, f2, d2 = w13.shape
+    f = f2 // 2
+    dev = xq.device
+    if out is None:
+        hq = torch.empty(rows, f, dtype=_U8, device=dev)
+        sh = torch.empty(f // 128, rows, dtype=_F32, device=dev)
+        y_rows = torch.empty(rows, d, dtype=_BF16, device=dev)
+    else:
+        hq, sh, y_rows = out
+    lib = load()
+    ws, wsb = WS.get(lib.moe_swiglu_ws_bytes(rows, d, f), dev)
+    call("moe_swiglu_fp8_fwd", _ptr(xq), _ptr(sx), T, _ptr(row_token), _ptr(offsets), rows,
+         _ptr(w13), _ptr(s13), _ptr(w2), _ptr(s2), S, d, f, _ptr(hq), _ptr(sh), _ptr(y_rows),
+         _ptr(status), ws, wsb, _stream())
+    return hq, sh, y_rows
+
+
+def combine(y_rows, row_of, gate, shared_row_base, status=None, out=None):
+    """BF16 y [T, d] = shared + sum_k gate * expert rows (FP32 accumulation)."""
+    _check(y_rows, _BF16, "y_rows", 2)
+    _check(row_of, _I32, "row_of", 2)
+    _check(gate, _F32, "gate", 2)
+    T, K = row_of.shape
+    d = y_rows.shape[1]
+    y = out if out is not None else torch.empty(T, d, dtype=_BF16, device=y_rows.device)
+    call("moe_combine", _ptr(y_rows), y_rows.shape[0], _ptr(row_of), _ptr(gate), T, K, d,
+         int(shared_row_base), _ptr(y), _ptr(status), _stream())
+    return y

@@ -1,0 +1,220 @@
+/*
+ * moe_fp8.h -- C-ABI of libmoe_fp8.so: the forward pass of one DeepSeek-V3 MoE FFN
+ * layer with FP8 E4M3 block-scaled experts, for NVIDIA B300 (sm_103a).
+ *
+ * The layer, in the order the entry points run it:
+ *   moe_router_logits     z = x . E^T                       (router, kept above FP8)
+ *   moe_route             sigmoid, bias for selection, group limit, top-k, gates
+ *   moe_permute           (token, slot) pairs -> expert-contiguous rows
+ *   fp8_quant_1x128       x -> E4M3 with one FP32 scale per 1x128 tile
+ *   moe_swiglu_fp8_fwd    grouped gate/up GEMM + SwiGLU + requantise, grouped down GEMM
+ *   moe_combine           y_t = shared_t + sum_k g_tk * expert_out
+ *   moe_bias_update       aux-loss-free bias step after the forward
+ * plus fp8_blockscaled_grouped_gemm (the GEMM on its own, dense when G = 1) and two
+ * setup helpers that prepare weights (fp8_quant_128x128, moe_router_split_bf16).
+ *
+ * Conventions shared by every entry point
+ *   - Every data pointer is a DEVICE pointer owned by the caller.  The library never
+ *     allocates device memory; scratch space comes from the caller through (ws,
+ *     ws_bytes), sized by moe_workspace_bytes() or the per-call *_ws_bytes() helpers.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t passed as void*; NULL is
+ *     the legacy default stream) and never synchronises the host.
+ *   - Return value: MOE_OK or a negative MOE_ERR_* code for errors found on the host
+ *     (arguments, launch failures).  Errors found on the device (bad indices in device
+ *     data, a bounded wait that expired) are written to the caller's `dev_status`
+ *     (int32 on the device, 0 = OK) where a call takes one; read it after a sync.
+ *     The first device error wins; later ones do not overwrite it.
+ *   - Results are deterministic: the same inputs give the same bits on every run.
+ *   - FP8 is E4M3 in the finite-number convention ("fn": max 448, no infinity, NaN =
+ *     0x7F/0xFF), stored as uint8.  BF16 is stored as uint16 bit patterns.
+ *   - Scales are FP32 dequantisation multipliers: x_hat = s * decode(q).
+ *       activation scales (1x128 tiles):  s[cols/128][rows]   (K-block-major)
+ *       weight scales (128x128 blocks):   s[G][N/128][K/128]
+ *
+ * Sources, cited by page title and section:
+ *   [book]  "DeepSeek-V3" book (slop-6tp.pages.dev/papers-html/dsv3): ch. 7 "Fine-grained
+ *           and Shared Experts", ch. 8 "Routing and Load Balancing", ch. 15 "Moving
+ *           Tokens to Experts", ch. 16 "Understanding FP8 Numbers", ch. 17 "The Actual
+ *           Mixed-precision Pipeline".
+ *   [sum]   "DeepSeek-V3" summary (deepseek-2024.kryvik.com): core ideas 1 (DeepSeekMoE,
+ *           node-limited routing), 2 (auxiliary-loss-free load balancing), 6 (FP8 mixed
+ *           precision (a)-(d)).
+ *   [pfd]   "DeepSeek-V3: the recipe, and the interconnect that shaped it"
+ *           (paperfordummies.in): "The one formula", "Auxiliary-loss-free balancing",
+ *           "FP8: the other half of the byte reduction".
+ */
+#ifndef MOE_FP8_H
+#define MOE_FP8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------------------ */
+#define MOE_OK                   0
+#define MOE_ERR_INVALID_ARG     -1  /* null pointer, misaligned pointer, bad dimension   */
+#define MOE_ERR_UNSUPPORTED     -2  /* valid but outside what the kernels implement      */
+#define MOE_ERR_CUDA            -3  /* a CUDA runtime/driver call or a launch failed     */
+#define MOE_ERR_DEVICE_TIMEOUT  -4  /* device: a bounded wait inside a kernel expired    */
+#define MOE_ERR_WORKSPACE       -5  /* ws is NULL or ws_bytes is too small               */
+#define MOE_ERR_DEVICE_DATA     -6  /* device: index data out of range / inconsistent    */
+
+/* Static description of a status code (never NULL). */
+const char* moe_status_string(int status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int moe_version(void);
+
+/* ---- router ------------------------------------------------------------------------ */
+
+/* Router logits z[t][i] = sum_k x[t][k] * e_i[k], FP32 result.
+ * The router is one of the places the method keeps above FP8 ([book] ch. 17 "High-
+ * precision exceptions", "Router precision has discrete consequences"; [sum] core
+ * idea 6).  x is BF16 [T][d] (row pitch d).  The FP32 centroids E [E][d] arrive split
+ * into two BF16 planes, w_hilo = [hi; lo] with hi = bf16(E), lo = bf16(E - hi)
+ * (moe_router_split_bf16), so the products run on BF16 tensor cores with FP32
+ * accumulation and E keeps 16 significant bits.
+ * Limits: d % 128 == 0, E % 16 == 0, E <= 256, T >= 0.  ws: moe_router_logits_ws_bytes.
+ * z: FP32 [T][E]. */
+int moe_router_logits(const uint16_t* x, int T, int d, const uint16_t* w_hilo, int E,
+                      float* z, void* ws, size_t ws_bytes, void* stream);
+size_t moe_router_logits_ws_bytes(int T, int d, int E);
+
+/* Setup helper (not on the timed path): split FP32 centroids [E][d] into the two BF16
+ * planes moe_router_logits takes: w_hilo[0][i][k] = bf16_rn(w), w_hilo[1][i][k] =
+ * bf16_rn(w - hi).  n = E * d elements. */
+int moe_router_split_bf16(const float* w, long long n, uint16_t* w_hilo, void* stream);
+
+/* Route every token ([sum] core ideas 1-2; [book] ch. 7 "The router's affinity scores",
+ * "Selecting and combining experts"; ch. 8 "V3's routing-only bias", "Restricting
+ * target nodes"):
+ *   s_i  = sigmoid(z_i)            (skipped when scores_are_affinities != 0)
+ *   c_i  = s_i + bias_i            selection score; the bias never reaches the gate
+ *   group score = sum of the group_topn largest c in the group (added in descending
+ *                 order); the topk_groups best groups are kept
+ *   idx  = the K largest c among experts of kept groups, listed in descending c
+ *   gate_k = s_idx_k / (s_idx_0 + ... + s_idx_{K-1}) * route_scale
+ * Ties in every ranking go to the lower index.  All arithmetic is FP32; divisions are
+ * IEEE round-to-nearest.  With scores_are_affinities the results are bit-identical to
+ * the plain definition above; from logits, sigmoid uses expf.
+ * scores: FP32 [T][E]; bias: FP32 [E]; topk_idx: int32 [T][K]; topk_gate: FP32 [T][K].
+ * Limits: E % n_groups == 0, n_groups <= 32, E <= 1024, 1 <= topk_groups <= n_groups,
+ * 1 <= group_topn <= E/n_groups, 1 <= K <= min(32, topk_groups*E/n_groups). */
+int moe_route(const float* scores, int scores_are_affinities, const float* bias,
+              int T, int E, int n_groups, int topk_groups, int group_topn, int K,
+              float route_scale, int32_t* topk_idx, float* topk_gate, void* stream);
+
+/* ---- dispatch metadata ------------------------------------------------------------- */
+
+/* Group the T*K (token, slot) pairs by expert ([book] ch. 15 "What dispatch must do";
+ * ch. 7 "Batches change what is active"; no token is dropped, [sum] core idea 1).
+ * A stable counting sort keyed by expert: rows of segment e are ordered by token.
+ * When include_shared != 0 the shared expert is segment E: rows T*K + t hold token t.
+ * Outputs (int32):
+ *   counts[E]            pairs per routed expert
+ *   offsets[E+2]         offsets[e] = first row of segment e; offsets[E] = T*K;
+ *                        offsets[E+1] = T*K + (include_shared ? T : 0)
+ *   row_token[T*K (+T)]  token held by each row
+ *   row_of[T][K]         row holding pair (t, k)
+ * An index outside [0, E) sets MOE_ERR_DEVICE_DATA in dev_status (outputs undefined).
+ * Limits: E <= 1024, K <= 32.  ws: moe_permute_ws_bytes. */
+int moe_permute(const int32_t* topk_idx, int T, int K, int E, int include_shared,
+                int32_t* counts, int32_t* offsets, int32_t* row_token, int32_t* row_of,
+                int32_t* dev_status, void* ws, size_t ws_bytes, void* stream);
+size_t moe_permute_ws_bytes(int T, int K, int E);
+
+/* ---- FP8 quantisation -------------------------------------------------------------- */
+
+/* Quantise BF16 x [rows][cols] (row pitch ldx elements) to E4M3 with one FP32 scale per
+ * 1x128 tile ([sum] core idea 6(a),(d); [book] ch. 16 "V3's grouping", "Online scales",
+ * "Scaling a group"):  amax = max|x| over the tile; s = amax / 448 (IEEE division);
+ * q = E4M3_rn_satfinite(x / s); amax == 0 gives s = 1, q = 0.
+ * q: uint8 [rows][cols]; scale: FP32 [cols/128][rows].  cols % 128 == 0, ldx >= cols,
+ * x 16-byte aligned with ldx % 8 == 0. */
+int fp8_quant_1x128(const uint16_t* x, int rows, int cols, int ldx, uint8_t* q,
+                    float* scale, void* stream);
+
+/* Setup helper: quantise FP32 w [rows][cols] in 128x128 blocks, same scale rule.
+ * q: uint8 [rows][cols]; scale: FP32 [rows/128][cols/128].  rows, cols % 128 == 0. */
+int fp8_quant_128x128(const float* w, int rows, int cols, uint8_t* q, float* scale,
+                      void* stream);
+
+/* ---- FP8 block-scaled grouped GEMM ------------------------------------------------- */
+
+/* C[r][n] = sum_kb sA[kb][r'] * sB[g][n/128][kb] * sum_{k in kb} A[r'][k] * B[g][n][k]
+ * for every row r of segment g (seg_offsets[g] <= r < seg_offsets[g+1]), with
+ * r' = a_rows ? a_rows[r] : r.  Each 128-deep K block is summed on the tensor cores,
+ * then scaled and added into FP32 ("promotion" every 128 elements of K: [sum] core idea
+ * 6(b); [book] ch. 16 "Scales along the GEMM inner dimension", "Periodic high-precision
+ * promotion").  C is BF16 (round to nearest even), row pitch ldc.
+ *   A:  uint8 [M_a][K] (M_a = M when a_rows is NULL, else the rows a_rows refers to),
+ *   sA: FP32 [K/128][M_a];  B: uint8 [G][N][K];  sB: FP32 [G][N/128][K/128];
+ *   seg_offsets: int32 [G+1] on the device, non-decreasing, seg_offsets[0] = 0,
+ *                seg_offsets[G] <= M;  a_rows: int32 [M] or NULL;  C: [M][ldc].
+ * G = 1 with seg_offsets = {0, M} is the dense GEMM.
+ * Limits: N % 128 == 0, K % 128 == 0, 1 <= G <= 1024, ldc % 8 == 0, A/B/C 16-byte
+ * aligned.  ws: fp8_grouped_gemm_ws_bytes (non-zero only when a_rows != NULL). */
+int fp8_blockscaled_grouped_gemm(const uint8_t* A, const float* sA, int M_a,
+                                 const int32_t* a_rows, const uint8_t* B, const float* sB,
+                                 const int32_t* seg_offsets, int G, int M, int N, int K,
+                                 uint16_t* C, int ldc, int32_t* dev_status,
+                                 void* ws, size_t ws_bytes, void* stream);
+size_t fp8_grouped_gemm_ws_bytes(int M, int K, int has_a_rows);
+
+/* ---- experts ----------------------------------------------------------------------- */
+
+/* SwiGLU experts on FP8 rows, one segment per expert ([book] ch. 2 "RMSNorm and
+ * SwiGLU", ch. 7 "What one expert computes"; [sum] core idea 6):
+ *   rows r of segment e take token row_token[r] of xq (quantised 1x128);
+ *   [G | U] = xq_rows . w13_e^T   (grouped block-scaled GEMM, FP32 results)
+ *   h = silu(G) * U               (FP32), requantised 1x128 along f -> hq, sh
+ *   y_rows = hq . w2_e^T          (grouped block-scaled GEMM, BF16 results)
+ * w13 interleaves the gate and up weights in 128-row blocks: rows [256j, 256j+128) of
+ * expert e are gate rows [128j, 128j+128) and rows [256j+128, 256j+256) the matching up
+ * rows, so every 256-column output tile holds matching gate and up columns.
+ *   xq: uint8 [T][d]; sx: FP32 [d/128][T]; row_token: int32 [rows]; offsets: int32
+ *   [n_segments+1] (device), offsets[n_segments] <= rows;
+ *   w13: uint8 [n_segments][2f][d]; s13: FP32 [n_segments][2f/128][d/128];
+ *   w2: uint8 [n_segments][d][f];   s2: FP32 [n_segments][d/128][f/128];
+ *   hq: uint8 [rows][f]; sh: FP32 [f/128][rows]; y_rows: BF16 [rows][d].
+ * Rows past offsets[n_segments] are not written.
+ * Limits: d % 128 == 0, f % 128 == 0, 1 <= n_segments <= 1024.
+ * ws: moe_swiglu_ws_bytes. */
+int moe_swiglu_fp8_fwd(const uint8_t* xq, const float* sx, int T, const int32_t* row_token,
+                       const int32_t* offsets, int rows, const uint8_t* w13,
+                       const float* s13, const uint8_t* w2, const float* s2,
+                       int n_segments, int d, int f, uint8_t* hq, float* sh,
+                       uint16_t* y_rows, int32_t* dev_status, void* ws, size_t ws_bytes,
+                       void* stream);
+size_t moe_swiglu_ws_bytes(int rows, int d, int f);
+
+/* ---- combine and bias update ------------------------------------------------------- */
+
+/* y[t] = bf16( y_rows[shared_row_base + t] + sum_{k=0..K-1} gate[t][k] * y_rows[row_of[t][k]] )
+ * accumulated in FP32 in exactly that order ([book] ch. 7 "Selecting and combining
+ * experts", ch. 15 "What combine must do", ch. 17 "FP8 dispatch, BF16 combine").
+ * shared_row_base < 0: no shared expert.  The residual is not added.
+ * y_rows: BF16 [n_rows][d]; row_of: int32 [T][K]; gate: FP32 [T][K]; y: BF16 [T][d].
+ * A row index outside [0, n_rows) sets MOE_ERR_DEVICE_DATA in dev_status and leaves that
+ * token's output unwritten.  d % 8 == 0, 1 <= K <= 32, y_rows and y 16-byte aligned. */
+int moe_combine(const uint16_t* y_rows, int n_rows, const int32_t* row_of,
+                const float* gate, int T, int K, int d, int shared_row_base, uint16_t* y,
+                int32_t* dev_status, void* stream);
+
+/* Aux-loss-free bias step ([sum] core idea 2; [book] ch. 8 "The feedback update";
+ * [pfd] "Auxiliary-loss-free balancing"):
+ *   bias[i] += gamma * sign(T*K/E - counts[i]),   sign(0) = 0,
+ * with the comparison done exactly in integers (T*K - E*counts[i]). */
+int moe_bias_update(float* bias, const int32_t* counts, int E, int T, int K, float gamma,
+                    void* stream);
+
+/* Workspace large enough for every call of one layer forward with these sizes. */
+size_t moe_workspace_bytes(int T, int K, int E, int d, int f);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_FP8_H */

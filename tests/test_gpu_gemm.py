@@ -1,0 +1,151 @@
+"""GPU parity of the tcgen05 block-scaled grouped GEMM (through the C-ABI) against the
+oracle's exact definition: dense and grouped, ragged and empty segments, a half-width
+last N tile, gathered A rows, and the five full-size sweep shapes on sampled rows."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from fp8_block_scaled_bias_b300 import ops
+from tolerance import assert_close, bf16_to_f32
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _codes(rows, cols, seed):
+    return workloads.gen_fp8_codes(rows, cols, sub_seed=seed)
+
+
+def _run(A, sA, B, sB, seg, M, a_rows=None):
+    st = ops.new_status(DEV)
+    C = ops.grouped_gemm(A.to(DEV), sA.to(DEV), B.to(DEV), sB.to(DEV),
+                         torch.tensor(seg, dtype=torch.int32, device=DEV), M,
+                         a_rows=None if a_rows is None else torch.tensor(a_rows, dtype=torch.int32,
+                                                                         device=DEV),
+                         status=st)
+    torch.cuda.synchronize()
+    assert ops.status_value(st) == 0
+    return bf16_to_f32(C)
+
+
+def _ref(A, sA, B, sB, seg, a_rows=None):
+    A, sA, B, sB = (t.numpy() for t in (A, sA, B, sB))
+    M = seg[-1]
+    out = np.zeros((M, B.shape[1]), np.float64)
+    for g in range(len(seg) - 1):
+        r0, r1 = seg[g], seg[g + 1]
+        if r1 == r0:
+            continue
+        rows = np.arange(r0, r1) if a_rows is None else np.asarray(a_rows[r0:r1])
+        out[r0:r1] = oracle.blockscaled_gemm(A[rows], sA[:, rows], B[g], sB[g])
+    return out
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 256, 128), (128, 256, 128), (200, 256, 512),
+                                   (300, 512, 1024), (129, 384, 256)])
+def test_dense_gemm(M, N, K):
+    A, B = _codes(M, K, 1), _codes(N, K, 2)
+    sA = workloads.gen_scales((K // 128, M), sub_seed=3)
+    sB = workloads.gen_scales((1, N // 128, K // 128), sub_seed=4)
+    C = _run(A, sA, B[None], sB, [0, M], M)
+    assert_close(C, _ref(A, sA, B[None], sB, [0, M]), what=f"dense {M}x{N}x{K}")
+
+
+def test_grouped_ragged_segments():
+    counts = [0, 130, 1, 256, 77, 0, 128]
+    seg = np.concatenate([[0], np.cumsum(counts)]).tolist()
+    M, N, K, G = seg[-1], 384, 256, len(counts)
+    A = _codes(M, K, 5)
+    sA = workloads.gen_scales((K // 128, M), sub_seed=6)
+    B = _codes(G * N, K, 7).view(G, N, K)
+    sB = workloads.gen_scales((G, N // 128, K // 128), sub_seed=8)
+    C = _run(A, sA, B, sB, seg, M)
+    assert_close(C, _ref(A, sA, B, sB, seg), what="grouped")
+
+
+def test_grouped_rows_past_last_segment_untouched():
+    seg = [0, 100, 100, 150]
+    M, N, K = 300, 256, 128
+    A = _codes(M, K, 9)
+    sA = workloads.gen_scales((K // 128, M), sub_seed=10)
+    B = _codes(3 * N, K, 11).view(3, N, K)
+    sB = workloads.gen_scales((3, N // 128, K // 128), sub_seed=12)
+    C = torch.full((M, N), 7.0, dtype=torch.bfloat16, device=DEV)
+    ops.grouped_gemm(A.to(DEV), sA.to(DEV), B.to(DEV), sB.to(DEV),
+                     torch.tensor(seg, dtype=torch.int32, device=DEV), M, out=C)
+    C = bf16_to_f32(C)
+    assert (C[150:] == 7.0).all()
+    assert_close(C[:150], _ref(A, sA, B, sB, seg), what="prefix rows")
+
+
+def test_grouped_with_gathered_rows():
+    T, K, N = 90, 256, 256
+    rng = np.random.default_rng(0)
+    a_rows = np.concatenate([rng.permutation(T)[:50], rng.permutation(T)[:70], np.arange(T)])
+    seg = [0, 50, 120, 120 + T]
+    A = _codes(T, K, 13)
+    sA = workloads.gen_scales((K // 128, T), sub_seed=14)
+    B = _codes(3 * N, K, 15).view(3, N, K)
+    sB = workloads.gen_scales((3, N // 128, K // 128), sub_seed=16)
+    C = _run(A, sA, B, sB, seg, len(a_rows), a_rows=a_rows)
+    assert_close(C, _ref(A, sA, B, sB, seg, a_rows), what="gathered")
+
+
+def test_bad_segment_table_is_reported():
+    A = torch.zeros(64, 128, dtype=torch.uint8, device=DEV)
+    sA = torch.ones(1, 64, device=DEV)
+    B = torch.zeros(2, 256, 128, dtype=torch.uint8, device=DEV)
+    sB = torch.ones(2, 2, 1, device=DEV)
+    st = ops.new_status(DEV)
+    ops.grouped_gemm(A, sA, B, sB, torch.tensor([0, 40, 30], dtype=torch.int32, device=DEV), 64,
+                     status=st)
+    assert ops.status_value(st) == -6
+    st = ops.new_status(DEV)
+    ops.grouped_gemm(A, sA, B, sB, torch.tensor([0, 40, 65], dtype=torch.int32, device=DEV), 64,
+                     status=st)
+    assert ops.status_value(st) == -6
+
+
+def test_closed_form_all_ones():
+    M, N, K = 256, 256, 1024
+    A = torch.full((M, K), 0x38, dtype=torch.uint8)          # E4M3 1.0
+    B = torch.full((1, N, K), 0x38, dtype=torch.uint8)
+    C = _run(A, torch.ones(K // 128, M), B, torch.ones(1, N // 128, K // 128), [0, M], M)
+    assert (C == K).all()
+
+
+@pytest.mark.parametrize("M,N,K", workloads.GEMM_SWEEP)
+def test_sweep_shape_sampled_rows(M, N, K):
+    """Full-size sweep shape, same launch as the bench; 128 seeded rows checked against
+    the oracle over every column."""
+    A = _codes(M, K, 21)
+    B = _codes(N, K, 22)
+    sA = workloads.gen_scales((K // 128, M), sub_seed=23)
+    sB = workloads.gen_scales((1, N // 128, K // 128), sub_seed=24)
+    C = _run(A, sA, B[None], sB, [0, M], M)
+    rows = np.sort(np.random.default_rng(M + N + K).choice(M, 128, replace=False))
+    rows[0], rows[-1] = 0, M - 1
+    ref = oracle.blockscaled_gemm(A.numpy()[rows], sA.numpy()[:, rows], B.numpy(), sB.numpy()[0])
+    assert_close(C[rows], ref, what=f"sweep {M}x{N}x{K}")
+
+
+def test_sweep_recipe_normal_operands():
+    """The sweep's own recipe: A, B ~ N(0,1), each side quantises them itself."""
+    M, N, K = 4096, 7168, 2048
+    a = workloads.gen_normal(M, K, sub_seed=31)
+    b = workloads.gen_normal(N, K, sub_seed=32)
+    qa, sa = ops.quant_1x128(a.to(torch.bfloat16).to(DEV))
+    qb, sb = ops.quant_128x128(b.to(DEV))
+    C = bf16_to_f32(ops.grouped_gemm(qa, sa, qb[None], sb[None],
+                                     torch.tensor([0, M], dtype=torch.int32, device=DEV), M))
+    rows = np.random.default_rng(1).choice(M, 64, replace=False)
+    qa_r, sa_r = oracle.quant_1x128(a.to(torch.bfloat16).float().numpy()[rows])
+    qb_r, sb_r = oracle.quant_128x128(b.numpy())
+    ref = oracle.blockscaled_gemm(qa_r, sa_r, qb_r, sb_r)
+    assert_close(C[rows], ref, what="N(0,1) recipe")
+    exact = a.to(torch.bfloat16).double().numpy()[rows] @ b.double().numpy().T
+    # FP8 quantisation error against the unquantised product: a few percent of RMS
+    assert np.abs(C[rows] - exact).mean() / np.sqrt((exact ** 2).mean()) < 0.05

@@ -1,0 +1,200 @@
+"""GPU parity of the whole MoE layer forward against the oracle.
+
+Tiny shape: every intermediate and the output, routed from identical logits (routing
+bit-exact) and from the GPU's own router logits.  V3, decode and skewed shapes: the
+router decisions of every token, and the outputs of sampled tokens computed one by one
+by the oracle from the same synthetic weights."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from fp8_block_scaled_bias_b300 import MoELayer, make_weights, ops
+from tolerance import assert_close, bf16_to_f32, routing_margin
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _oracle_experts(cfg):
+    ex = []
+    for e in range(cfg.E + 1):
+        w = [t.numpy() for t in workloads.gen_expert_f32(cfg, e, device="cuda")]
+        ex.append(tuple(a for m in w for a in oracle.quant_128x128(m)))
+    return ex
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    cfg = workloads.TINY
+    w = make_weights(cfg, DEV)
+    x = workloads.gen_x(cfg)
+    return cfg, w, x, _oracle_experts(cfg)
+
+
+def test_tiny_weights_quantised_like_oracle(tiny):
+    cfg, w, x, ex = tiny
+    for e in (0, 7, cfg.E):
+        q1, s1, q3, s3, q2, s2 = ex[e]
+        from fp8_block_scaled_bias_b300 import interleave_gate_up
+        w13, s13 = interleave_gate_up(torch.from_numpy(q1), torch.from_numpy(s1),
+                                      torch.from_numpy(q3), torch.from_numpy(s3))
+        assert np.array_equal(w.w13[e].cpu().numpy(), w13.numpy())
+        assert np.array_equal(w.s13[e].cpu().numpy(), s13.numpy())
+        assert np.array_equal(w.w2[e].cpu().numpy(), q2)
+        assert np.array_equal(w.s2[e].cpu().numpy(), s2)
+
+
+def _compare_tiny(cfg, layer, ref, x):
+    T, K = cfg.T, cfg.K
+    for name in ("idx", "gate", "counts", "offsets", "row_token", "row_of", "xq", "sx"):
+        got = getattr(layer, name).cpu().numpy()
+        assert np.array_equal(got, ref[name]), name
+    # h is requantised from FP32 partial sums: decoded values agree to FP8 rounding
+    hq = oracle.dequant_1x128(layer.hq.cpu().numpy(), layer.sh.cpu().numpy())
+    hr = oracle.dequant_1x128(ref["hq"], ref["sh"])
+    assert_close(hq, hr, max_rel=0.07, mae=5e-3, what="h")
+    assert_close(bf16_to_f32(layer.y_rows), ref["Y"], what="expert rows")
+    assert_close(bf16_to_f32(layer.y), ref["y"], what="layer output")
+
+
+def test_tiny_layer_from_identical_logits(tiny):
+    cfg, w, x, ex = tiny
+    g = torch.Generator().manual_seed(5)
+    logits = (torch.randn(cfg.T, cfg.E, generator=g) * 1.5).float()
+    layer = MoELayer(cfg, w)
+    layer.forward(x.to(DEV), logits=logits.to(DEV))
+    torch.cuda.synchronize()
+    layer.check_status()
+    ref = oracle.moe_layer(x.float().numpy(), w.centroids.cpu().numpy(), w.bias.cpu().numpy(),
+                           ex, cfg.n_groups, cfg.topk_groups, cfg.K, logits=logits.numpy())
+    _compare_tiny(cfg, layer, ref, x)
+
+
+def test_tiny_layer_full_path(tiny):
+    cfg, w, x, ex = tiny
+    layer = MoELayer(cfg, w)
+    layer.forward(x.to(DEV))
+    torch.cuda.synchronize()
+    layer.check_status()
+    ref = oracle.moe_layer(x.float().numpy(), w.centroids.cpu().numpy(), w.bias.cpu().numpy(),
+                           ex, cfg.n_groups, cfg.topk_groups, cfg.K)
+    z = layer.z.cpu().numpy()
+    assert np.abs(z - ref["z"]).max() <= 1e-4 * np.abs(ref["z"]).max()
+    if np.array_equal(layer.idx.cpu().numpy(), ref["idx"]):
+        _compare_tiny(cfg, layer, ref, x)
+    else:                                     # a near-tie flipped: compare unaffected tokens
+        same = (layer.idx.cpu().numpy() == ref["idx"]).all(1)
+        assert same.mean() > 0.99
+        assert_close(bf16_to_f32(layer.y)[same], ref["y"][same], what="layer output")
+
+
+def test_layer_is_deterministic(tiny):
+    cfg, w, x, _ = tiny
+    layer = MoELayer(cfg, w)
+    xd = x.to(DEV)
+    first = layer.forward(xd).clone()
+    for _ in range(3):
+        assert torch.equal(layer.forward(xd), first)
+
+
+def test_residual_flag(tiny):
+    cfg, w, x, _ = tiny
+    layer = MoELayer(cfg, w)
+    xd = x.to(DEV)
+    y = layer.forward(xd).clone()
+    assert torch.equal(layer.forward(xd, residual=True), y + xd)
+
+
+# ---- V3-shaped configurations: all routing decisions, sampled outputs -------------------
+
+@pytest.fixture(scope="module")
+def v3_weights():
+    return make_weights(workloads.V3, DEV)
+
+
+def _routing_agrees(cfg, layer, x, bias):
+    """The oracle's router on the oracle's own logits; returns the tokens whose decisions
+    match and checks that every mismatch sits on a near-tie."""
+    z_ref = oracle.router_logits(x.float().numpy(), layer.w.centroids.cpu().numpy())
+    z = layer.z.cpu().numpy()
+    assert np.abs(z - z_ref).max() <= 2e-5 * np.abs(z_ref).max()
+    i_ref, g_ref = oracle.route(z_ref, bias, cfg.n_groups, cfg.topk_groups, cfg.group_topn, cfg.K)
+    idx = layer.idx.cpu().numpy()
+    same = (idx == i_ref).all(1)
+    c = (oracle.sigmoid_f32(z_ref) + bias[None]).astype(np.float32)
+    for t in np.nonzero(~same)[0]:
+        # a flipped decision must sit within the logits' rounding difference
+        assert routing_margin(c[t], i_ref[t], cfg.n_groups, cfg.topk_groups,
+                              cfg.group_topn) < 1e-4
+    assert same.mean() >= 0.998
+    g = layer.gate.cpu().numpy()
+    assert np.abs(g[same] - g_ref[same]).max() <= 1e-5
+    return same, i_ref
+
+
+def _sampled_outputs(cfg, layer, x, bias, tokens):
+    w32 = lambda e: tuple(t.numpy() for t in workloads.gen_expert_f32(cfg, e, device="cuda"))
+    part = oracle.moe_layer_tokens(tokens, x.float().numpy()[tokens],
+                                   layer.w.centroids.cpu().numpy(), bias, w32, cfg.n_groups,
+                                   cfg.topk_groups, cfg.K)
+    return part
+
+
+def _check_config(cfg, w, n_sample):
+    x = workloads.gen_x(cfg)
+    layer = MoELayer(cfg, w)
+    layer.forward(x.to(DEV))
+    torch.cuda.synchronize()
+    layer.check_status()
+    bias = w.bias.cpu().numpy()
+    same, i_ref = _routing_agrees(cfg, layer, x, bias)
+    # permutation invariants on the GPU's own routing
+    counts = layer.counts.cpu().numpy()
+    assert counts.sum() == cfg.T * cfg.K
+    assert np.array_equal(counts, np.bincount(layer.idx.cpu().numpy().ravel(), minlength=cfg.E))
+    if same.all():
+        ref = oracle.permute(i_ref, cfg.E)
+        for got, want in zip((layer.counts, layer.offsets, layer.row_token, layer.row_of), ref):
+            assert np.array_equal(got.cpu().numpy(), want)
+    rng = np.random.default_rng(cfg.T)
+    cand = np.nonzero(same)[0]
+    tokens = sorted(rng.choice(cand, n_sample, replace=False).tolist())
+    part = _sampled_outputs(cfg, layer, x, bias, tokens)
+    y = bf16_to_f32(layer.y)[tokens]
+    assert_close(y, part["y"], what=f"{cfg.name} sampled tokens")
+    return layer
+
+
+def test_v3_layer(v3_weights):
+    _check_config(workloads.V3, v3_weights, n_sample=4)
+
+
+def test_decode_layer(v3_weights):
+    _check_config(workloads.DECODE, v3_weights, n_sample=4)
+
+
+def test_skewed_layer_and_bias_update(v3_weights):
+    cfg = workloads.SKEWED
+    w = v3_weights
+    saved = w.bias.clone()
+    try:
+        w.bias.copy_(workloads.gen_bias(cfg).to(DEV))
+        layer = _check_config(cfg, w, n_sample=3)
+        counts = layer.counts.cpu().numpy()
+        assert counts.max() / counts.mean() > 4          # Zipf-shaped popularity
+        before = w.bias.cpu().numpy().copy()
+        layer.bias_update(0.001)
+        assert np.array_equal(w.bias.cpu().numpy(),
+                              oracle.bias_update(before, counts, cfg.T, cfg.K, 0.001))
+        x = workloads.gen_x(cfg).to(DEV)
+        layer.forward(x)
+        torch.cuda.synchronize()
+        layer.check_status()
+        c2 = layer.counts.cpu().numpy()
+        over = counts * cfg.E > cfg.T * cfg.K
+        assert c2[over].sum() <= counts[over].sum()      # overloaded experts lose load
+    finally:
+        w.bias.copy_(saved)
