@@ -53,14 +53,17 @@ def moe_layer(x, centroids, bias, experts, n_groups, topk_groups, k, route_scale
 
 
 def moe_layer_tokens(tokens, x_rows, centroids, bias, expert_weights_f32, n_groups,
-                     topk_groups, k, route_scale=1.0):
+                     topk_groups, k, route_scale=1.0, expert_quantised=None):
     """Layer output for a few tokens only (for shapes too large to run whole).
 
     Rows of a segment never interact, so a token's output depends only on its own row,
     its chosen experts and the shared expert.  ``x_rows`` float32 [n, d] holds the
     tokens' inputs; ``expert_weights_f32(e)`` returns float32 (w1 [f,d], w3 [f,d],
     w2 [d,f]) for expert e (e = E is the shared expert); the oracle quantises them
-    itself.  Returns dict(idx [n,k], gate [n,k], y [n,d], s [n,E]).
+    itself.  ``expert_quantised(e)``, when given, returns expert e already quantised
+    with ``quant_128x128`` as (w1q, s1, w3q, s3, w2q, s2) and replaces that step (it lets a
+    caller run the quantisation of many experts in parallel).
+    Returns dict(idx [n,k], gate [n,k], y [n,d], s [n,E]).
     """
     x_rows = np.asarray(x_rows, dtype=np.float32)
     E = centroids.shape[0]
@@ -70,6 +73,8 @@ def moe_layer_tokens(tokens, x_rows, centroids, bias, expert_weights_f32, n_grou
     cache = {}
 
     def quantised(e):
+        if expert_quantised is not None:
+            return expert_quantised(e)
         if e not in cache:
             w1, w3, w2 = expert_weights_f32(e)
             cache[e] = (*quant_128x128(w1), *quant_128x128(w3), *quant_128x128(w2))

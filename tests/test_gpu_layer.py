@@ -5,6 +5,8 @@ bit-exact) and from the GPU's own router logits.  V3, decode and skewed shapes: 
 router decisions of every token, and the outputs of sampled tokens computed one by one
 by the oracle from the same synthetic weights."""
 
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -135,12 +137,32 @@ def _routing_agrees(cfg, layer, x, bias):
     return same, i_ref
 
 
-def _sampled_outputs(cfg, layer, x, bias, tokens):
-    w32 = lambda e: tuple(t.numpy() for t in workloads.gen_expert_f32(cfg, e, device="cuda"))
-    part = oracle.moe_layer_tokens(tokens, x.float().numpy()[tokens],
-                                   layer.w.centroids.cpu().numpy(), bias, w32, cfg.n_groups,
-                                   cfg.topk_groups, cfg.K)
-    return part
+_POOL = None
+
+
+def _pool():
+    """Process pool for the oracle's weight quantisation (spawned, never forked)."""
+    global _POOL
+    if _POOL is None:
+        import concurrent.futures as cf
+        import multiprocessing as mp
+        _POOL = cf.ProcessPoolExecutor(max_workers=max(1, min(24, (os.cpu_count() or 2) - 1)),
+                                       mp_context=mp.get_context("spawn"))
+    return _POOL
+
+
+def _sampled_outputs(cfg, layer, x, bias, tokens, i_ref):
+    """Oracle outputs of the sampled tokens; the experts they use are generated from the
+    same seeds and quantised by the oracle (in parallel worker processes)."""
+    need = sorted(set(int(e) for t in tokens for e in i_ref[t]) | {cfg.E})
+    mats = []
+    for e in need:
+        mats.extend(t.numpy() for t in workloads.gen_expert_f32(cfg, e, device="cuda"))
+    quant = list(_pool().map(oracle.quant_128x128, mats))
+    q = {e: tuple(a for j in range(3) for a in quant[3 * i + j]) for i, e in enumerate(need)}
+    return oracle.moe_layer_tokens(tokens, x.float().numpy()[tokens],
+                                   layer.w.centroids.cpu().numpy(), bias, None, cfg.n_groups,
+                                   cfg.topk_groups, cfg.K, expert_quantised=q.__getitem__)
 
 
 def _check_config(cfg, w, n_sample):
@@ -162,7 +184,7 @@ def _check_config(cfg, w, n_sample):
     rng = np.random.default_rng(cfg.T)
     cand = np.nonzero(same)[0]
     tokens = sorted(rng.choice(cand, n_sample, replace=False).tolist())
-    part = _sampled_outputs(cfg, layer, x, bias, tokens)
+    part = _sampled_outputs(cfg, layer, x, bias, tokens, i_ref)
     y = bf16_to_f32(layer.y)[tokens]
     assert_close(y, part["y"], what=f"{cfg.name} sampled tokens")
     return layer

@@ -74,3 +74,7 @@ def test_per_token_variant_matches_whole_layer():
     assert (part["idx"] == out["idx"][toks]).all()
     assert (part["gate"] == out["gate"][toks]).all()
     assert (part["y"] == out["y"][toks]).all()
+    # pre-quantised experts given by the caller take the same path
+    part2 = oracle.moe_layer_tokens(toks, x[toks], cen, bias, None, cfg.n_groups,
+                                    cfg.topk_groups, cfg.K, expert_quantised=experts.__getitem__)
+    assert (part2["y"] == part["y"]).all() and (part2["idx"] == part["idx"]).all()
