@@ -1,0 +1,465 @@
+"""Benchmark of the MoE FFN layer forward (DeepSeek-V3 shape) on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--config v3|decode|skewed|tiny|sweep]
+
+One step is one pass of the whole hot path over one batch: router logits, routing,
+permutation, 1x128 quantisation, row gather, gate/up grouped GEMM with fused SwiGLU and
+requantisation, down grouped GEMM, combine, and the aux-loss-free bias update.  Rank 0
+prints one JSON line.  Under torchrun each rank runs its own replica on its own GPU and
+its own tokens (weak scaling, no collective on the data path); the time is the max over
+ranks.
+
+--impl reference times the CPU oracle (numpy, float64) on a bounded sample of the same
+workload: each step routes one token and runs its experts, one token at a time.
+
+Inputs are synthetic and seeded (workloads.py).  The expert weights (11.3 GB of E4M3)
+are larger than L2 and are streamed from HBM every step, so no L2 flush is needed
+between steps.
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np
+import torch
+
+import workloads
+
+METRIC = "MoE-layer fwd tokens/s & FP8 TFLOPS at V3 shape; % of B300 FP8/HBM roofline"
+GAMMA = 0.001
+# the kernel sources the committed DRAM-traffic figure was measured with
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gate_up_v3_traffic.json")
+GEMM_SOURCES = ["fp8_block_scaled_bias_b300/csrc/gemm_fp8.cu",
+                "fp8_block_scaled_bias_b300/csrc/common.cuh"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", choices=["v3", "decode", "skewed", "tiny", "sweep"], default="v3")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ---- distributed plumbing ----------------------------------------------------------------
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return rank, world, torch.device("cuda", torch.cuda.current_device())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---- peaks, clocks -----------------------------------------------------------------------
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        m = json.load(open(p))
+        return {"hbm_gbs": float(m["hbm_gbs"]), "bf16_tflops": float(m["bf16_tflops"]),
+                "bf16_tflops_sustained": float(m.get("bf16_tflops_sustained", m["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
+                "source": "fallback"}
+
+
+class ClockSampler:
+    """Samples SM clock and clock-event reasons through NVML while the timed region runs."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x2: "applications_clocks_setting", 0x100: "display_clock_setting"}
+
+    def __init__(self, index, period=0.01):
+        self.samples, self.reasons, self.period = [], set(), period
+        self._stop = threading.Event()
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+        except Exception:
+            self.nv = None
+            self.max_mhz = None
+
+    def _run(self):
+        nv = self.nv
+        while not self._stop.is_set():
+            try:
+                self.samples.append(nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM))
+                r = nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                for bit, name in self.REASONS.items():
+                    if r & bit:
+                        self.reasons.add(name)
+            except Exception:
+                pass
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.nv is not None:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self.nv is not None:
+            self._stop.set()
+            self._t.join()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+                    "samples": 0}
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(self.reasons), "samples": len(self.samples)}
+
+
+def gemm_source_hash():
+    h = hashlib.sha256()
+    for p in GEMM_SOURCES:
+        h.update(open(os.path.join(ROOT, p), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic():
+    """DRAM bytes per gate/up launch from the committed ncu summary, if it was taken with
+    the current kernel source; else None."""
+    try:
+        t = json.load(open(TRAFFIC_FILE))
+    except Exception:
+        return None
+    if t.get("kernel_source_sha256_16") != gemm_source_hash():
+        return None
+    return t.get("dram_bytes_per_launch_v3")
+
+
+# ---- our arm -----------------------------------------------------------------------------
+
+def gate_up_bytes(cfg, counts_np, T):
+    """Algorithmic HBM bytes of one gate/up launch: the weights and scales of every expert
+    segment with at least one row, the gathered FP8 rows and their scales read once, and
+    the FP8 h rows and scales written once."""
+    E, d, f = cfg.E, cfg.d, cfg.f
+    active = int((counts_np > 0).sum()) + 1                    # + the shared expert
+    rows = T * cfg.K + T
+    w = active * (2 * f * d + (2 * f // 128) * (d // 128) * 4)
+    a = rows * d + rows * (d // 128) * 4
+    h = rows * f + rows * (f // 128) * 4
+    return w + a + h
+
+
+def down_bytes(cfg, counts_np, T):
+    E, d, f = cfg.E, cfg.d, cfg.f
+    active = int((counts_np > 0).sum()) + 1
+    rows = T * cfg.K + T
+    return active * (d * f + (d // 128) * (f // 128) * 4) + rows * f + rows * (f // 128) * 4 + \
+        rows * d * 2
+
+
+def run_layer(args, cfg, rank, world, dev):
+    from fp8_block_scaled_bias_b300 import MoELayer, make_weights
+    from fp8_block_scaled_bias_b300.layer import MoELayer as _L
+
+    T = cfg.T
+    w = make_weights(cfg, dev)
+    x_host = workloads.gen_x(cfg, base_seed=rank).pin_memory()
+    x = x_host.to(dev)
+    layer = MoELayer(cfg, w)
+    stages = list(_L.STAGE_LAUNCHES) + ["bias_update"]
+    launches_per_step = sum(_L.STAGE_LAUNCHES.values()) + 1
+
+    def step(marks=None):
+        mk = None
+        if marks is not None:
+            def mk(name):
+                e = torch.cuda.Event(enable_timing=True)
+                e.record()
+                marks.append((name, e))
+        layer.forward(x, mark=mk)
+        layer.bias_update(GAMMA)
+        if mk:
+            mk("bias_update")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    layer.check_status()
+
+    # device-resident timed region
+    all_marks = []
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clocks:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(args.steps):
+            marks = [("start", None)]
+            ev = torch.cuda.Event(enable_timing=True)
+            ev.record()
+            marks[0] = ("start", ev)
+            step(marks)
+            all_marks.append(marks)
+        t1.record()
+        torch.cuda.synchronize()
+    barrier(world)
+    ms_total = max_over_ranks(t0.elapsed_time(t1), world)
+    layer.check_status()
+    stage_ms = {s: 0.0 for s in stages}
+    for marks in all_marks:
+        for (n0, e0), (n1, e1) in zip(marks[:-1], marks[1:]):
+            stage_ms[n1] += e0.elapsed_time(e1)
+    stage_ms = {k: v / args.steps for k, v in stage_ms.items()}
+
+    # end to end through the public API: pinned host x in, pinned host y out, every step
+    y_host = torch.empty(T, cfg.d, dtype=torch.bfloat16).pin_memory()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        x.copy_(x_host, non_blocking=True)
+        layer.forward(x)
+        layer.bias_update(GAMMA)
+        y_host.copy_(layer.y, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    ms_e2e = max_over_ranks(e0.elapsed_time(e1), world)
+    layer.check_status()
+
+    counts = layer.counts.cpu().numpy()
+    return dict(ms_total=ms_total, stage_ms=stage_ms, ms_e2e=ms_e2e, clocks=clocks.summary(),
+                counts=counts, launches=launches_per_step * args.steps,
+                h2d=x_host.numel() * 2, d2h=y_host.numel() * 2, layer=layer, weights=w, x=x_host)
+
+
+def cpu_baseline(cfg, cen, bias, x_host, n_tokens=4, steps=None):
+    """The oracle, as it stands, on a bounded sample: n_tokens tokens of the workload, one
+    at a time through oracle.moe_layer_tokens (routing in float64/float32, every expert
+    block-scaled GEMM exact in float64).  Expert weights are generated from the same seeds
+    and quantised by the oracle in spawned worker processes before timing starts."""
+    import concurrent.futures as cf
+    import multiprocessing as mp
+
+    from threadpoolctl import threadpool_limits
+
+    import oracle
+
+    rng = np.random.default_rng(7)
+    tokens = sorted(rng.choice(cfg.T, n_tokens, replace=False).tolist())
+    xr = x_host.float().numpy()[tokens]
+    z = oracle.router_logits(xr, cen)
+    idx, _ = oracle.route(z, bias, cfg.n_groups, cfg.topk_groups, cfg.group_topn, cfg.K)
+    need = sorted(set(int(e) for r in idx for e in r) | {cfg.E})
+    mats = []
+    for e in need:
+        mats.extend(t.numpy() for t in workloads.gen_expert_f32(cfg, e, device="cuda"))
+    workers = max(1, min(16, (os.cpu_count() or 2) - 1))
+    with cf.ProcessPoolExecutor(max_workers=workers, mp_context=mp.get_context("spawn")) as pool:
+        quant = list(pool.map(oracle.quant_128x128, mats))
+    q = {e: tuple(a for j in range(3) for a in quant[3 * i + j]) for i, e in enumerate(need)}
+    del mats
+    steps = steps or n_tokens
+    times = []
+    with threadpool_limits(1):
+        for s in range(steps):
+            t = tokens[s % n_tokens]
+            t0 = time.perf_counter()
+            oracle.moe_layer_tokens([t], x_host.float().numpy()[[t]], cen, bias, None,
+                                    cfg.n_groups, cfg.topk_groups, cfg.K,
+                                    expert_quantised=q.__getitem__)
+            times.append(time.perf_counter() - t0)
+    return dict(value=len(times) / sum(times), times=times, tokens=tokens, cores=1)
+
+
+def main_ours(args, cfg, rank, world, dev):
+    pk = peaks()
+    r = run_layer(args, cfg, rank, world, dev)
+    T, K = cfg.T, args.steps
+    ms_step = r["ms_total"] / K
+    tokens_s = T * world * K / (r["ms_total"] / 1e3)
+    flops = cfg.flops()
+    st = r["stage_ms"]
+    gu_bytes = gate_up_bytes(cfg, r["counts"], T)
+    gu_ms = st["gate_up"]
+    fp8_peak = 2.0 * pk["bf16_tflops_sustained"]
+    gemm_ms = st["gate_up"] + st["down"]
+    out = {
+        "metric": METRIC, "value": round(tokens_s, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8_e4m3", "data": "synthetic",
+        "config": {"workload": f"DeepSeek-V3-shape MoE layer fwd ({cfg.name}): T={T}, "
+                               f"d_model={cfg.d}, {cfg.E} routed experts in {cfg.n_groups} "
+                               f"groups, top-{cfg.K} of at most {cfg.topk_groups} groups, "
+                               f"d_ffn={cfg.f}, 1 shared expert; bias update gamma={GAMMA}",
+                   "tokens_per_gpu": T, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (all expert weights streamed from HBM each step)"},
+        "fp8_tflops": round(flops * world * K / (r["ms_total"] / 1e3) / 1e12, 1),
+        "gemm_fp8_tflops": round(flops / (gemm_ms / 1e3) / 1e12, 1),
+        "roofline": {"kernel": "fp8_gemm_kernel<SwiGLU> (gate/up grouped GEMM)", "bound": "hbm",
+                     "achieved": round(gu_bytes / (gu_ms / 1e3) / 1e9, 1),
+                     "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(gu_bytes / (gu_ms / 1e3) / 1e9 / pk["hbm_gbs"], 4),
+                     "traffic": committed_traffic(), "algorithmic_bytes": gu_bytes,
+                     "peak_source": pk["source"]},
+        "layer_roofline": {
+            "hbm_bytes": gu_bytes + down_bytes(cfg, r["counts"], T),
+            "hbm_frac": round((gu_bytes + down_bytes(cfg, r["counts"], T)) / (ms_step / 1e3)
+                              / 1e9 / pk["hbm_gbs"], 4),
+            "tensor_frac_of_fp8_sustained": round(flops / (ms_step / 1e3) / 1e12 / fp8_peak, 4),
+            "fp8_peak_tflops": fp8_peak, "fp8_peak_note": "2 x measured sustained bf16 (nominal fp8/bf16 ratio)"},
+        "stage_ms": {k: round(v, 4) for k, v in st.items()},
+        "e2e": {"value": round(T * world * K / (r["ms_e2e"] / 1e3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+        "gpu_launches": r["launches"],
+        "clocks": r["clocks"],
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cb = cpu_baseline(cfg, r["weights"].centroids.cpu().numpy(),
+                          r["weights"].bias.cpu().numpy(), r["x"])
+        out["cpu_baseline"] = {"value": round(cb["value"], 4), "unit": "tokens/s", "cores": cb["cores"],
+                               "kind": "oracle",
+                               "sample": f"{len(cb['times'])} tokens of this workload, one at a time "
+                                         f"through the numpy oracle (tokens {cb['tokens']}); expert "
+                                         f"weights pre-quantised outside the timing"}
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def main_reference(args, cfg, rank, world, dev):
+    if rank != 0:
+        return
+    # the oracle needs only the router and the experts of the sampled tokens, all from
+    # the same seeded generators as our arm
+    cen = workloads.gen_centroids(cfg).numpy()
+    bias = workloads.gen_bias(cfg).numpy()
+    x_host = workloads.gen_x(cfg)
+    cb = cpu_baseline(cfg, cen, bias, x_host, n_tokens=4, steps=args.warmup + args.steps)
+    times = cb["times"][args.warmup:] or cb["times"]
+    value = len(times) / sum(times)
+    out = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * sum(times) / len(times), 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"DeepSeek-V3-shape MoE layer fwd ({cfg.name}): T={cfg.T}, "
+                               f"d_model={cfg.d}, {cfg.E} routed experts in {cfg.n_groups} "
+                               f"groups, top-{cfg.K}, d_ffn={cfg.f}, 1 shared expert",
+                   "tokens_per_gpu": cfg.T, "parallelism": "none (host CPU)"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": cb["cores"],
+                         "kind": "oracle",
+                         "sample": "each step: one token of the workload through the numpy "
+                                   f"oracle (cycling tokens {cb['tokens']})"},
+        "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main_sweep(args, rank, dev):
+    """Standalone FP8 block-scaled GEMM sweep (one JSON line per shape); L2 is flushed
+    between timed launches."""
+    from fp8_block_scaled_bias_b300 import ops
+    pk = peaks()
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    for (M, N, K) in workloads.GEMM_SWEEP:
+        a = workloads.gen_normal(M, K, sub_seed=31, device="cuda").to(torch.bfloat16)
+        b = workloads.gen_normal(N, K, sub_seed=32, device="cuda")
+        qa, sa = ops.quant_1x128(a)
+        qb, sb = ops.quant_128x128(b)
+        del a, b
+        seg = torch.tensor([0, M], dtype=torch.int32, device=dev)
+        C = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        run = lambda: ops.grouped_gemm(qa, sa, qb[None], sb[None], seg, M, out=C)
+        for _ in range(args.warmup):
+            run()
+        ts = []
+        with ClockSampler(dev.index) as clocks:
+            for _ in range(args.steps):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                run()
+                e1.record()
+                ts.append((e0, e1))
+            torch.cuda.synchronize()
+        ms = statistics.median(e0.elapsed_time(e1) for e0, e1 in ts)
+        tf = 2.0 * M * N * K / (ms / 1e3) / 1e12
+        fp8_peak = 2.0 * pk["bf16_tflops"]
+        print(json.dumps({"metric": "FP8 block-scaled GEMM TFLOPS", "value": round(tf, 1),
+                          "unit": "TFLOP/s", "config": {"workload": f"GEMM sweep M={M} N={N} K={K}",
+                                                        "l2": "flushed between launches"},
+                          "ms": round(ms, 4), "steps": args.steps,
+                          "roofline": {"bound": "tensor", "achieved": round(tf, 1),
+                                       "peak": fp8_peak, "unit": "TFLOP/s",
+                                       "frac": round(tf / fp8_peak, 4),
+                                       "peak_note": "2 x measured burst bf16"},
+                          "clocks": clocks.summary()}), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        if rank != 0:
+            return
+        cfg = workloads.CONFIGS["v3" if args.config in ("sweep",) else args.config]
+        torch.cuda.set_device(0)
+        main_reference(args, cfg, 0, 1, torch.device("cuda", 0))
+        return
+    rank, world, dev = dist_setup()
+    import fp8_block_scaled_bias_b300 as pkg
+    if not os.path.exists(pkg.LIB_PATH):
+        from fp8_block_scaled_bias_b300.build import build
+        build()
+    pkg.load()
+    if args.config == "sweep":
+        main_sweep(args, rank, dev)
+    else:
+        main_ours(args, workloads.CONFIGS[args.config], rank, world, dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -34,6 +34,8 @@ SIGNATURES = {
     "moe_swiglu_fp8_fwd": (_I, [_P, _P, _I, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P,
                                 _P, _P, _SZ, _P]),
     "moe_swiglu_ws_bytes": (_SZ, [_I, _I, _I]),
+    "moe_gather_rows_fp8": (_I, [_P, _P, _I, _P, _P, _I, _I, _P, _P, _P, _P]),
+    "moe_gate_up_fp8": (_I, [_P, _P, _P, _I, _P, _P, _I, _I, _I, _P, _P, _P, _P]),
     "moe_combine": (_I, [_P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _P]),
     "moe_bias_update": (_I, [_P, _P, _I, _I, _I, _F, _P]),
     "moe_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),

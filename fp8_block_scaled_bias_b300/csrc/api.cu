@@ -217,6 +217,34 @@ int moe_swiglu_fp8_fwd(const uint8_t* xq, const float* sx, int T, const int32_t*
   return moe::launch_fp8_gemm(down, moe::kEpiBF16, s);
 }
 
+int moe_gather_rows_fp8(const uint8_t* src, const float* src_scale, int src_rows,
+                        const int32_t* rows, const int32_t* row_limit, int n_rows, int cols,
+                        uint8_t* dst, float* dst_scale, int32_t* dev_status, void* stream) {
+  if (src_rows < 0 || n_rows < 0 || cols <= 0 || cols % 128 != 0) return MOE_ERR_INVALID_ARG;
+  if (n_rows == 0) return MOE_OK;
+  if (!src || !src_scale || !rows || !dst || !dst_scale || !aligned16(src) || !aligned16(dst))
+    return MOE_ERR_INVALID_ARG;
+  return moe::launch_gather_rows_fp8(src, src_scale, src_rows, rows, row_limit, n_rows, cols, dst,
+                                     dst_scale, dev_status, as_stream(stream));
+}
+
+int moe_gate_up_fp8(const uint8_t* xq_rows, const float* sx_rows, const int32_t* offsets,
+                    int rows, const uint8_t* w13, const float* s13, int n_segments, int d, int f,
+                    uint8_t* hq, float* sh, int32_t* dev_status, void* stream) {
+  if (rows < 0 || d <= 0 || f <= 0 || d % 128 != 0 || f % 128 != 0 || n_segments < 1)
+    return MOE_ERR_INVALID_ARG;
+  const int st = check_gemm_dims(n_segments, rows, 2 * f, d);
+  if (st != MOE_OK) return st;
+  if (rows == 0) return MOE_OK;
+  if (!xq_rows || !sx_rows || !offsets || !w13 || !s13 || !hq || !sh) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(xq_rows) || !aligned16(w13) || !aligned16(hq)) return MOE_ERR_INVALID_ARG;
+  GemmArgs up{};
+  up.A = xq_rows; up.sA = sx_rows; up.B = w13; up.sB = s13; up.seg = offsets;
+  up.G = n_segments; up.M = rows; up.N = 2 * f; up.K = d;
+  up.hq = hq; up.sh = sh; up.status = dev_status;
+  return moe::launch_fp8_gemm(up, moe::kEpiSwiGLU, as_stream(stream));
+}
+
 // ---- combine, bias update, workspace -------------------------------------------------
 
 int moe_combine(const uint16_t* y_rows, int n_rows, const int32_t* row_of, const float* gate,

@@ -91,28 +91,50 @@ class MoELayer:
         self.row_of = emp(T, K, dt=torch.int32)
         self.xq = emp(T, d, dt=torch.uint8)
         self.sx = emp(d // 128, T)
+        self.xq_rows = emp(self.rows, d, dt=torch.uint8)
+        self.sx_rows = emp(d // 128, self.rows)
         self.hq = emp(self.rows, f, dt=torch.uint8)
         self.sh = emp(f // 128, self.rows)
         self.y_rows = emp(self.rows, d, dt=torch.bfloat16)
         self.y = emp(T, d, dt=torch.bfloat16)
         self.status = ops.new_status(dev)
-        self.launches_per_forward = 10     # logits, route, permute x3, quant, gather, GEMM x2, combine
+        self.seg_end = self.offsets[cfg.E + 1:cfg.E + 2]     # device int32: rows in use
 
-    def forward(self, x, logits=None, residual=False):
-        """x BF16 [T, d] on the device -> y BF16 [T, d] (the layer's own buffer)."""
+    # kernel launches of one forward, by stage (bias_update adds one more)
+    STAGE_LAUNCHES = {"router_logits": 1, "route": 1, "permute": 3, "quant": 1, "gather": 1,
+                      "gate_up": 1, "down": 1, "combine": 1}
+
+    def forward(self, x, logits=None, residual=False, mark=None):
+        """x BF16 [T, d] on the device -> y BF16 [T, d] (the layer's own buffer).
+
+        ``mark(name)``, if given, is called after each stage's launches (the bench records
+        a CUDA event there)."""
         cfg, w = self.cfg, self.w
+        mark = mark or (lambda name: None)
         if logits is None:
             ops.router_logits(x, w.w_hilo, out=self.z)
             z = self.z
         else:
             z = logits
+        mark("router_logits")
         ops.route(z, w.bias, cfg.n_groups, cfg.topk_groups, cfg.K, out=(self.idx, self.gate))
+        mark("route")
         ops.permute(self.idx, cfg.E, True, self.status,
                     out=(self.counts, self.offsets, self.row_token, self.row_of))
+        mark("permute")
         ops.quant_1x128(x, out=(self.xq, self.sx))
-        ops.swiglu_fwd(self.xq, self.sx, self.row_token, self.offsets, self.rows, w.w13, w.s13,
-                       w.w2, w.s2, self.status, out=(self.hq, self.sh, self.y_rows))
+        mark("quant")
+        ops.gather_rows(self.xq, self.sx, self.row_token, self.seg_end, self.status,
+                        out=(self.xq_rows, self.sx_rows))
+        mark("gather")
+        ops.gate_up(self.xq_rows, self.sx_rows, self.offsets, w.w13, w.s13, self.status,
+                    out=(self.hq, self.sh))
+        mark("gate_up")
+        ops.grouped_gemm(self.hq, self.sh, w.w2, w.s2, self.offsets, self.rows,
+                         status=self.status, out=self.y_rows)
+        mark("down")
         ops.combine(self.y_rows, self.row_of, self.gate, self.T * cfg.K, self.status, out=self.y)
+        mark("combine")
         if residual:
             return self.y + x
         return self.y

@@ -209,6 +209,40 @@ def swiglu_fwd(xq, sx, row_token, offsets, rows, w13, s13, w2, s2, status=None, 
     return hq, sh, y_rows
 
 
+def gather_rows(src, src_scale, rows, row_limit=None, status=None, out=None):
+    """FP8 rows in a new order: dst[r] = src[rows[r]] with their 1x128 scales."""
+    _check(src, _U8, "src", 2)
+    _check(src_scale, _F32, "src_scale", 2)
+    _check(rows, _I32, "rows", 1)
+    n, cols = rows.numel(), src.shape[1]
+    if out is None:
+        dst = torch.empty(n, cols, dtype=_U8, device=src.device)
+        dsc = torch.empty(cols // 128, n, dtype=_F32, device=src.device)
+    else:
+        dst, dsc = out
+    call("moe_gather_rows_fp8", _ptr(src), _ptr(src_scale), src.shape[0], _ptr(rows),
+         _ptr(row_limit), n, cols, _ptr(dst), _ptr(dsc), _ptr(status), _stream())
+    return dst, dsc
+
+
+def gate_up(xq_rows, sx_rows, offsets, w13, s13, status=None, out=None):
+    """hq, sh = requantised silu(gate) * up over expert segments (rows in segment order)."""
+    for t, dt, n in ((xq_rows, _U8, "xq_rows"), (sx_rows, _F32, "sx_rows"),
+                     (offsets, _I32, "offsets"), (w13, _U8, "w13"), (s13, _F32, "s13")):
+        _check(t, dt, n)
+    rows, d = xq_rows.shape
+    S, f2, _ = w13.shape
+    f = f2 // 2
+    if out is None:
+        hq = torch.empty(rows, f, dtype=_U8, device=xq_rows.device)
+        sh = torch.empty(f // 128, rows, dtype=_F32, device=xq_rows.device)
+    else:
+        hq, sh = out
+    call("moe_gate_up_fp8", _ptr(xq_rows), _ptr(sx_rows), _ptr(offsets), rows, _ptr(w13),
+         _ptr(s13), S, d, f, _ptr(hq), _ptr(sh), _ptr(status), _stream())
+    return hq, sh
+
+
 def combine(y_rows, row_of, gate, shared_row_base, status=None, out=None):
     """BF16 y [T, d] = shared + sum_k gate * expert rows (FP32 accumulation)."""
     _check(y_rows, _BF16, "y_rows", 2)

@@ -191,6 +191,25 @@ int moe_swiglu_fp8_fwd(const uint8_t* xq, const float* sx, int T, const int32_t*
                        void* stream);
 size_t moe_swiglu_ws_bytes(int rows, int d, int f);
 
+/* The three steps of moe_swiglu_fp8_fwd as separate calls (same kernels), for callers
+ * that schedule or time them one by one:
+ *   moe_gather_rows_fp8  dst[r] = src[rows[r]] (an FP8 matrix of `cols` columns with its
+ *                        1x128 scales [cols/128][src_rows] -> [cols/128][n_rows]) for
+ *                        r < min(n_rows, *row_limit); row_limit is a device int32 (NULL:
+ *                        n_rows).  An index outside [0, src_rows) sets
+ *                        MOE_ERR_DEVICE_DATA.  cols % 128 == 0; src, dst 16-byte aligned.
+ *   moe_gate_up_fp8      hq, sh = requant_1x128( silu(G) * U ), [G | U] = xq_rows . w13_e^T
+ *                        per segment, xq_rows already in segment order ([rows][d], scales
+ *                        [d/128][rows]).  Layouts as in moe_swiglu_fp8_fwd.
+ *   the down projection is fp8_blockscaled_grouped_gemm(hq, sh, rows, NULL, w2, s2,
+ *   offsets, n_segments, rows, d, f, y_rows, d, ...). */
+int moe_gather_rows_fp8(const uint8_t* src, const float* src_scale, int src_rows,
+                        const int32_t* rows, const int32_t* row_limit, int n_rows, int cols,
+                        uint8_t* dst, float* dst_scale, int32_t* dev_status, void* stream);
+int moe_gate_up_fp8(const uint8_t* xq_rows, const float* sx_rows, const int32_t* offsets,
+                    int rows, const uint8_t* w13, const float* s13, int n_segments, int d,
+                    int f, uint8_t* hq, float* sh, int32_t* dev_status, void* stream);
+
 /* ---- combine and bias update ------------------------------------------------------- */
 
 /* y[t] = bf16( y_rows[shared_row_base + t] + sum_{k=0..K-1} gate[t][k] * y_rows[row_of[t][k]] )

@@ -73,6 +73,12 @@ def test_tiny_layer_from_identical_logits(tiny):
     ref = oracle.moe_layer(x.float().numpy(), w.centroids.cpu().numpy(), w.bias.cpu().numpy(),
                            ex, cfg.n_groups, cfg.topk_groups, cfg.K, logits=logits.numpy())
     _compare_tiny(cfg, layer, ref, x)
+    # the one-call expert entry point runs the same kernels: identical bits
+    hq, sh, y_rows = ops.swiglu_fwd(layer.xq, layer.sx, layer.row_token, layer.offsets,
+                                    layer.rows, w.w13, w.s13, w.w2, w.s2, layer.status)
+    torch.cuda.synchronize()
+    assert torch.equal(hq, layer.hq) and torch.equal(sh, layer.sh)
+    assert torch.equal(y_rows, layer.y_rows)
 
 
 def test_tiny_layer_full_path(tiny):
