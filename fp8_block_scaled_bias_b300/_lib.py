@@ -20,7 +20,7 @@ _LL = C.c_longlong
 SIGNATURES = {
     "moe_status_string": (C.c_char_p, [_I]),
     "moe_version": (_I, []),
-    "moe_router_logits": (_I, [_P, _I, _I, _P, _I, _P, _P, _SZ, _P]),
+    "moe_router_logits": (_I, [_P, _I, _I, _P, _I, _P, _P, _P, _SZ, _P]),
     "moe_router_logits_ws_bytes": (_SZ, [_I, _I, _I]),
     "moe_router_split_bf16": (_I, [_P, _LL, _P, _P]),
     "moe_route": (_I, [_P, _I, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P]),

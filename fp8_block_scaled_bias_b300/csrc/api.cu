@@ -47,14 +47,14 @@ size_t moe_router_logits_ws_bytes(int T, int d, int E) {
 }
 
 int moe_router_logits(const uint16_t* x, int T, int d, const uint16_t* w_hilo, int E,
-                      float* z, void* ws, size_t ws_bytes, void* stream) {
+                      float* z, int32_t* dev_status, void* ws, size_t ws_bytes, void* stream) {
   if (T < 0 || d <= 0 || E <= 0 || d % 128 != 0 || E % 16 != 0) return MOE_ERR_INVALID_ARG;
   if (E > 256) return MOE_ERR_UNSUPPORTED;
   if (T == 0) return MOE_OK;
   if (!x || !w_hilo || !z || !aligned16(x) || !aligned16(w_hilo)) return MOE_ERR_INVALID_ARG;
   const size_t need = moe::router_logits_ws_bytes(T, d, E);
   if (need > 0 && (!ws || ws_bytes < need)) return MOE_ERR_WORKSPACE;
-  return moe::launch_router_logits(x, T, d, w_hilo, E, z, ws, as_stream(stream));
+  return moe::launch_router_logits(x, T, d, w_hilo, E, z, dev_status, ws, as_stream(stream));
 }
 
 int moe_router_split_bf16(const float* w, long long n, uint16_t* w_hilo, void* stream) {

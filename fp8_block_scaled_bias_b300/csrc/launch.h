@@ -62,7 +62,7 @@ struct GemmArgs {
 int launch_fp8_gemm(const GemmArgs& a, GemmEpilogue epi, cudaStream_t stream);
 
 int launch_router_logits(const uint16_t* x, int T, int d, const uint16_t* w_hilo, int E,
-                         float* z, void* ws, cudaStream_t stream);
+                         float* z, int32_t* status, void* ws, cudaStream_t stream);
 size_t router_logits_ws_bytes(int T, int d, int E);
 int launch_router_split(const float* w, long long n, uint16_t* w_hilo, cudaStream_t stream);
 

@@ -1,67 +1,177 @@
-// Router logits z = x . E^T with FP32 accumulation.
+// Router logits z = x . E^T with FP32 accumulation, on tcgen05 BF16 tensor cores.
 //
 // The router is kept above FP8 ("DeepSeek-V3" book, ch. 17 "High-precision
 // exceptions", "Router precision has discrete consequences"; "DeepSeek-V3" summary,
 // core idea 6).  The FP32 centroids arrive as two BF16 planes hi + lo (16 significant
-// bits); x is BF16, so every product hi*x and lo*x is exact in FP32.
+// bits); x is BF16, so every product hi*x and lo*x is exact and both planes accumulate
+// into one FP32 TMEM accumulator: z = sum_k x_k hi_k + x_k lo_k.
 //
-// This kernel is a CUDA-core tiled GEMM: a 64-token x 64-expert block tile, 4x4 outputs
-// per thread, K staged through shared memory 32 at a time.
+// One CTA per 128-token x BN-expert tile (BN = min(64, E)); the whole K = d loop runs in
+// the CTA with a 6-stage TMA pipeline (x tile 128x64 BF16, hi and lo tiles BNx64).
+//   warp 0      TMA producer
+//   warp 1      TMEM allocation; one thread issues 8 MMAs (M128 N=BN K16) per 64-deep
+//               K block: 4 K steps on the hi plane and 4 on the lo plane
+//   warps 2..5  epilogue: TMEM -> registers -> z (FP32)
+#include <cuda.h>
+
 #include "common.cuh"
 #include "launch.h"
 
 namespace moe {
 
-namespace {
-constexpr int RT_M = 64, RT_N = 64, RT_K = 32;
+namespace rk {
+constexpr int BM = 128, BK = 64;                  // BK in BF16 elements = 128 bytes
+constexpr int MAX_BN = 64;
+constexpr int STAGES = 6;
+constexpr int A_BYTES = BM * BK * 2;              // 16 KB
+constexpr int B_BYTES = MAX_BN * BK * 2;          // 8 KB per plane
+constexpr int STAGE_BYTES = A_BYTES + 2 * B_BYTES;
+constexpr int THREADS = 192;
+constexpr uint32_t TMEM_COLS = 64;
+constexpr int OFF_BAR = STAGES * STAGE_BYTES;
+constexpr int OFF_MISC = OFF_BAR + (2 * STAGES + 2) * 8;
+constexpr int SMEM_ALLOC = OFF_MISC + 16 + 1024;
+static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
+}  // namespace rk
+
+struct RouterParams {
+  float* z;
+  int T, d, E, BN;
+  int32_t* status;
+};
+
+__global__ void __launch_bounds__(rk::THREADS, 1)
+    router_logits_kernel(const __grid_constant__ CUtensorMap tmX,
+                         const __grid_constant__ CUtensorMap tmW, const RouterParams p) {
+  using namespace rk;
+  extern __shared__ uint8_t router_smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(router_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + OFF_BAR;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  const uint32_t acc_bar = bar0 + 8u * (2 * STAGES);
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 1);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int BN = p.BN;
+  const int m0 = blockIdx.y * BM;
+  const int n0 = blockIdx.x * BN;
+  const int KB = p.d / BK;
+  const uint32_t stage_tx = A_BYTES + 2u * BN * BK * 2;
+
+  if (tid == 0) {
+    *abort_flag = 0;
+    for (int s = 0; s < STAGES; ++s) { mbar_init(full_bar(s), 1); mbar_init(empty_bar(s), 1); }
+    mbar_init(acc_bar, 1);
+    mbar_init(drain_bar, 1);
+    fence_barrier_init();
+    tma_prefetch_desc(&tmX);
+    tma_prefetch_desc(&tmW);
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      bool ok = true;
+      int kb = 0;
+      for (; kb < KB; ++kb) {
+        const int s = kb % STAGES;
+        const uint32_t ph = (kb / STAGES) & 1;
+        if (!mbar_wait(empty_bar(s), ph ^ 1, abort_flag, p.status)) { ok = false; break; }
+        const uint32_t st = sbase + s * STAGE_BYTES;
+        mbar_arrive_expect_tx(full_bar(s), stage_tx);
+        tma_load_2d(st, &tmX, kb * BK, m0, full_bar(s));
+        tma_load_2d(st + A_BYTES, &tmW, kb * BK, n0, full_bar(s));              // hi plane
+        tma_load_2d(st + A_BYTES + B_BYTES, &tmW, kb * BK, p.E + n0, full_bar(s));  // lo plane
+      }
+      if (!ok) {
+        const int first = kb > STAGES ? kb - STAGES : 0;
+        for (int i = first; i < kb; ++i) {
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(full_bar(i % STAGES), (i / STAGES) & 1))
+            if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = make_idesc(BM, BN, 1u, 1u);     // BF16 x BF16 -> F32
+      for (int kb = 0; kb < KB; ++kb) {
+        const int s = kb % STAGES;
+        const uint32_t ph = (kb / STAGES) & 1;
+        if (!mbar_wait(full_bar(s), ph, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t st = sbase + s * STAGE_BYTES;
+        const uint64_t adesc = smem_desc_sw128(st);
+        const uint64_t hdesc = smem_desc_sw128(st + A_BYTES);
+        const uint64_t ldesc = smem_desc_sw128(st + A_BYTES + B_BYTES);
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k) {       // 16 BF16 = 32 bytes per MMA: +2 encoded
+          mma_bf16(tmem_base, adesc + 2 * k, hdesc + 2 * k, idesc, (kb | k) ? 1u : 0u);
+          mma_bf16(tmem_base, adesc + 2 * k, ldesc + 2 * k, idesc, 1u);
+        }
+        mma_commit(empty_bar(s));
+      }
+      mma_commit(acc_bar);
+      mma_commit(drain_bar);
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(drain_bar, 0))
+        if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+    }
+  } else {
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    if (mbar_wait(acc_bar, 0, abort_flag, p.status)) {
+      tc_fence_after();
+      const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+      const int t = m0 + row;
+      for (int c = 0; c < BN; c += 32) {
+        uint32_t v[32];
+        if (BN - c >= 32) {
+          tmem_ld_32x32b_x32(tb + c, v);
+          tmem_ld_wait();
+          if (t < p.T) {
+            float4* dst = reinterpret_cast<float4*>(p.z + static_cast<long long>(t) * p.E + n0 + c);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                   __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+          }
+        } else {
+          // 16-column tail (BN = 16 or 48): load 32 columns, keep 16
+          tmem_ld_32x32b_x32(tb + c, v);     // columns c..c+31 lie inside the 64 allocated
+          tmem_ld_wait();
+          if (t < p.T) {
+            float4* dst = reinterpret_cast<float4*>(p.z + static_cast<long long>(t) * p.E + n0 + c);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                   __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
 }
 
-__global__ void __launch_bounds__(256) router_logits_simt_kernel(
-    const uint16_t* __restrict__ x, int T, int d, const uint16_t* __restrict__ w_hilo, int E,
-    float* __restrict__ z) {
-  __shared__ float xs[RT_K][RT_M + 4];
-  __shared__ float ws[RT_K][RT_N + 4];
-  const int t0 = blockIdx.y * RT_M, e0 = blockIdx.x * RT_N;
-  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-  const uint16_t* w_lo = w_hilo + static_cast<long long>(E) * d;
-  float acc[4][4] = {};
-  for (int k0 = 0; k0 < d; k0 += RT_K) {
-    // 64 rows x 32 k for x and for w: 2048 values each, 8 per thread
-    for (int i = threadIdx.x; i < RT_M * RT_K; i += 256) {
-      const int r = i / RT_K, k = i % RT_K;
-      const int t = t0 + r, e = e0 + r;
-      xs[k][r] = (t < T) ? bf16_bits_to_f32(x[static_cast<long long>(t) * d + k0 + k]) : 0.0f;
-      float wv = 0.0f;
-      if (e < E) {
-        const long long o = static_cast<long long>(e) * d + k0 + k;
-        wv = bf16_bits_to_f32(w_hilo[o]) + bf16_bits_to_f32(w_lo[o]);   // exact
-      }
-      ws[k][r] = wv;
-    }
-    __syncthreads();
-#pragma unroll 8
-    for (int k = 0; k < RT_K; ++k) {
-      float a[4], b[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) { a[i] = xs[k][ty * 4 + i]; b[i] = ws[k][tx * 4 + i]; }
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = __fmaf_rn(a[i], b[j], acc[i][j]);
-    }
-    __syncthreads();
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int t = t0 + ty * 4 + i;
-    if (t >= T) continue;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int e = e0 + tx * 4 + j;
-      if (e < E) z[static_cast<long long>(t) * E + e] = acc[i][j];
-    }
-  }
-}
+bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* ptr,
+                    uint64_t inner, uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
+                    uint32_t box_outer);   // runtime.cu
 
 size_t router_logits_ws_bytes(int T, int d, int E) {
   (void)T; (void)d; (void)E;
@@ -69,11 +179,26 @@ size_t router_logits_ws_bytes(int T, int d, int E) {
 }
 
 int launch_router_logits(const uint16_t* x, int T, int d, const uint16_t* w_hilo, int E,
-                         float* z, void* ws, cudaStream_t stream) {
+                         float* z, int32_t* status, void* ws, cudaStream_t stream) {
+  using namespace rk;
   (void)ws;
   if (T == 0) return MOE_OK;
-  dim3 grid((E + RT_N - 1) / RT_N, (T + RT_M - 1) / RT_M);
-  router_logits_simt_kernel<<<grid, 256, 0, stream>>>(x, T, d, w_hilo, E, z);
+  int BN = 16;                                   // widest multiple of 16 <= 64 dividing E
+  for (int b = MAX_BN; b >= 16; b -= 16)
+    if (E % b == 0) { BN = b; break; }
+  if (E % BN != 0) return MOE_ERR_UNSUPPORTED;
+  CUtensorMap tmX, tmW;
+  if (!encode_tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, d, T, 2ull * d, BK, BM))
+    return MOE_ERR_CUDA;
+  if (!encode_tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w_hilo, d, 2ull * E, 2ull * d, BK,
+                      BN))
+    return MOE_ERR_CUDA;
+  RouterParams p{z, T, d, E, BN, status};
+  if (cudaFuncSetAttribute(router_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           SMEM_ALLOC) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  dim3 grid(E / BN, (T + BM - 1) / BM);
+  router_logits_kernel<<<grid, THREADS, SMEM_ALLOC, stream>>>(tmX, tmW, p);
   return check_launch();
 }
 

@@ -112,7 +112,7 @@ class MoELayer:
         cfg, w = self.cfg, self.w
         mark = mark or (lambda name: None)
         if logits is None:
-            ops.router_logits(x, w.w_hilo, out=self.z)
+            ops.router_logits(x, w.w_hilo, self.status, out=self.z)
             z = self.z
         else:
             z = logits

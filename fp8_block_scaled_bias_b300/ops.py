@@ -72,7 +72,7 @@ def router_split_bf16(w):
     return out
 
 
-def router_logits(x, w_hilo, out=None):
+def router_logits(x, w_hilo, status=None, out=None):
     """z [T, E] FP32 = x [T, d] (BF16) . (hi + lo)^T."""
     _check(x, _BF16, "x", 2)
     _check(w_hilo, _BF16, "w_hilo", 3)
@@ -83,7 +83,8 @@ def router_logits(x, w_hilo, out=None):
     z = out if out is not None else torch.empty(T, E, dtype=_F32, device=x.device)
     lib = load()
     ws, wsb = WS.get(lib.moe_router_logits_ws_bytes(T, d, E), x.device)
-    call("moe_router_logits", _ptr(x), T, d, _ptr(w_hilo), E, _ptr(z), ws, wsb, _stream())
+    call("moe_router_logits", _ptr(x), T, d, _ptr(w_hilo), E, _ptr(z), _ptr(status), ws, wsb,
+         _stream())
     return z
 
 

@@ -84,7 +84,7 @@ def test_host_argument_checks_need_no_gpu():
     assert lib.moe_combine(P, 8, P, P, 4, 33, 128, -1, P, None, None) == -2
     assert lib.moe_combine(P, 8, P, P, 4, 4, 100, -1, P, None, None) == -1
     # router logits: E above the tensor-core tile
-    assert lib.moe_router_logits(P, 4, 128, P, 512, P, None, 0, None) == -2
+    assert lib.moe_router_logits(P, 4, 128, P, 512, P, None, None, 0, None) == -2
     assert lib.moe_bias_update(None, P, 16, 4, 2, 0.001, None) == -1
 
 

@@ -245,3 +245,37 @@ def test_combine_reports_bad_row():
     st = ops.new_status(DEV)
     ops.combine(Y, row_of, gate, -1, st)
     assert ops.status_value(st) == -6
+
+
+# ---- router logits -------------------------------------------------------------------
+
+@pytest.mark.parametrize("T,d,E", [(1, 128, 16), (130, 512, 16), (256, 512, 48), (300, 384, 80),
+                                   (4096, 7168, 256)])
+def test_router_logits_against_oracle(T, d, E):
+    """z on BF16 tensor cores from the hi/lo split: within 2^-14 of sum_k |x_k e_k| of the
+    exact product (dropping the lo plane would miss by about 2^-9 of it)."""
+    g = torch.Generator().manual_seed(T + d + E)
+    x = torch.randn(T, d, generator=g)
+    x[:, :4] *= 30.0                                   # outlier channels
+    x = x.to(torch.bfloat16)
+    cen = (torch.randn(E, d, generator=g) * 0.02).float()
+    hilo = ops.router_split_bf16(cen.to(DEV))
+    st = ops.new_status(DEV)
+    z = ops.router_logits(x.to(DEV), hilo, st).cpu().numpy()
+    assert ops.status_value(st) == 0
+    xf = x.float().numpy().astype(np.float64)
+    z_ref = xf @ cen.numpy().astype(np.float64).T
+    bound = 2.0 ** -14 * (np.abs(xf) @ np.abs(cen.numpy().astype(np.float64)).T) + 1e-30
+    assert (np.abs(z - z_ref) <= bound).all()
+    assert np.array_equal(oracle.router_logits(x.float().numpy(), cen.numpy()),
+                          z_ref.astype(np.float32))
+
+
+def test_router_split_planes():
+    w = torch.tensor([[1.0, 1.0 + 2 ** -10, -3.14159265, 1e-30, 0.0, 65504.0, -2.0 ** -130, 7.0]],
+                     dtype=torch.float32).repeat(1, 16)
+    hl = ops.router_split_bf16(w.to(DEV)).cpu()
+    hi, lo = hl[0].float(), hl[1].float()
+    assert torch.equal(hi, w.to(torch.bfloat16).float())
+    assert torch.equal(lo, (w - hi).to(torch.bfloat16).float())
+    assert ((hi + lo - w).abs() <= 2.0 ** -16 * w.abs() + 1e-38).all()
