@@ -271,16 +271,54 @@ def run_layer(args, cfg, rank, world, dev):
                 h2d=x_host.numel() * 2, d2h=y_host.numel() * 2, layer=layer, weights=w, x=x_host)
 
 
+def _oracle_token_times(payload):
+    """Worker (spawned with one BLAS/OpenMP thread): time oracle.moe_layer_tokens on one
+    token per step."""
+    import oracle
+    cfg, tokens, xr, cen, bias, q, steps = payload
+    times = []
+    for s in range(steps):
+        i = s % len(tokens)
+        t0 = time.perf_counter()
+        oracle.moe_layer_tokens([tokens[i]], xr[i:i + 1], cen, bias, None, cfg.n_groups,
+                                cfg.topk_groups, cfg.K, expert_quantised=q.__getitem__)
+        times.append(time.perf_counter() - t0)
+    return times
+
+
+class _WorkerThreads:
+    """Within this block, newly started processes run numpy with `n` threads (the
+    variables are read when a process imports numpy; this process is not affected)."""
+    KEYS = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
+
+    def __init__(self, n):
+        self.n = n
+
+    def __enter__(self):
+        self.old = {k: os.environ.get(k) for k in self.KEYS}
+        for k in self.KEYS:
+            os.environ[k] = str(self.n)
+
+    def __exit__(self, *a):
+        for k, v in self.old.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+
+
+def _spawn_pool(workers):
+    import concurrent.futures as cf
+    import multiprocessing as mp
+    return cf.ProcessPoolExecutor(max_workers=workers, mp_context=mp.get_context("spawn"))
+
+
 def cpu_baseline(cfg, cen, bias, x_host, n_tokens=4, steps=None):
     """The oracle, as it stands, on a bounded sample: n_tokens tokens of the workload, one
     at a time through oracle.moe_layer_tokens (routing in float64/float32, every expert
-    block-scaled GEMM exact in float64).  Expert weights are generated from the same seeds
-    and quantised by the oracle in spawned worker processes before timing starts."""
-    import concurrent.futures as cf
-    import multiprocessing as mp
-
-    from threadpoolctl import threadpool_limits
-
+    block-scaled GEMM exact in float64), in one process with one thread.  Expert weights
+    are generated from the same seeds and quantised by the oracle in spawned worker
+    processes before timing starts."""
     import oracle
 
     rng = np.random.default_rng(7)
@@ -291,22 +329,17 @@ def cpu_baseline(cfg, cen, bias, x_host, n_tokens=4, steps=None):
     need = sorted(set(int(e) for r in idx for e in r) | {cfg.E})
     mats = []
     for e in need:
-        mats.extend(t.numpy() for t in workloads.gen_expert_f32(cfg, e, device="cuda"))
+        mats.extend(t.cpu().numpy() for t in workloads.gen_expert_f32(cfg, e, device="cuda"))
     workers = max(1, min(16, (os.cpu_count() or 2) - 1))
-    with cf.ProcessPoolExecutor(max_workers=workers, mp_context=mp.get_context("spawn")) as pool:
-        quant = list(pool.map(oracle.quant_128x128, mats))
-    q = {e: tuple(a for j in range(3) for a in quant[3 * i + j]) for i, e in enumerate(need)}
-    del mats
-    steps = steps or n_tokens
-    times = []
-    with threadpool_limits(1):
-        for s in range(steps):
-            t = tokens[s % n_tokens]
-            t0 = time.perf_counter()
-            oracle.moe_layer_tokens([t], x_host.float().numpy()[[t]], cen, bias, None,
-                                    cfg.n_groups, cfg.topk_groups, cfg.K,
-                                    expert_quantised=q.__getitem__)
-            times.append(time.perf_counter() - t0)
+    with _WorkerThreads(1):
+        with _spawn_pool(workers) as pool:
+            quant = list(pool.map(oracle.quant_128x128, mats))
+        q = {e: tuple(a for j in range(3) for a in quant[3 * i + j]) for i, e in enumerate(need)}
+        del mats, quant
+        steps = steps or n_tokens
+        with _spawn_pool(1) as pool:
+            times = pool.submit(_oracle_token_times,
+                                (cfg, tokens, xr, cen, bias, q, steps)).result()
     return dict(value=len(times) / sum(times), times=times, tokens=tokens, cores=1)
 
 

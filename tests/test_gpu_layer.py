@@ -23,7 +23,7 @@ DEV = "cuda"
 def _oracle_experts(cfg):
     ex = []
     for e in range(cfg.E + 1):
-        w = [t.numpy() for t in workloads.gen_expert_f32(cfg, e, device="cuda")]
+        w = [t.cpu().numpy() for t in workloads.gen_expert_f32(cfg, e, device="cuda")]
         ex.append(tuple(a for m in w for a in oracle.quant_128x128(m)))
     return ex
 
@@ -163,7 +163,7 @@ def _sampled_outputs(cfg, layer, x, bias, tokens, i_ref):
     need = sorted(set(int(e) for t in tokens for e in i_ref[t]) | {cfg.E})
     mats = []
     for e in need:
-        mats.extend(t.numpy() for t in workloads.gen_expert_f32(cfg, e, device="cuda"))
+        mats.extend(t.cpu().numpy() for t in workloads.gen_expert_f32(cfg, e, device="cuda"))
     quant = list(_pool().map(oracle.quant_128x128, mats))
     q = {e: tuple(a for j in range(3) for a in quant[3 * i + j]) for i, e in enumerate(need)}
     return oracle.moe_layer_tokens(tokens, x.float().numpy()[tokens],
