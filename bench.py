@@ -49,7 +49,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", choices=["v3", "decode", "skewed", "tiny", "sweep"], default="v3")
+    ap.add_argument("--config", choices=["v3", "decode", "skewed", "tiny", "v3_e32", "sweep"],
+                    default="v3")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -105,9 +106,14 @@ class ClockSampler:
                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
                0x2: "applications_clocks_setting", 0x100: "display_clock_setting"}
 
+    SMI_FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.sw_power_cap,"
+                  "clocks_event_reasons.hw_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                  "clocks_event_reasons.hw_thermal_slowdown")
+
     def __init__(self, index, period=0.01):
-        self.samples, self.reasons, self.period = [], set(), period
+        self.samples, self.reasons, self.period, self.index = [], set(), period, index
         self._stop = threading.Event()
+        self.proc = None
         try:
             import pynvml
             pynvml.nvmlInit()
@@ -135,12 +141,37 @@ class ClockSampler:
         if self.nv is not None:
             self._t = threading.Thread(target=self._run, daemon=True)
             self._t.start()
+        else:                      # no NVML binding: sample with nvidia-smi instead
+            import subprocess
+            try:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.SMI_FIELDS,
+                     "--format=csv,noheader,nounits", "-lms", "20"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            except Exception:
+                self.proc = None
         return self
 
     def __exit__(self, *a):
         if self.nv is not None:
             self._stop.set()
             self._t.join()
+        elif self.proc is not None:
+            self.proc.terminate()
+            out, _ = self.proc.communicate(timeout=10)
+            names = ("sw_power_cap", "hw_slowdown", "sw_thermal_slowdown", "hw_thermal_slowdown")
+            for line in out.splitlines():
+                f = [v.strip() for v in line.split(",")]
+                if len(f) < 6:
+                    continue
+                try:
+                    self.samples.append(float(f[0]))
+                    self.max_mhz = float(f[1])
+                except ValueError:
+                    continue
+                for name, v in zip(names, f[2:6]):
+                    if v.lower() == "active":
+                        self.reasons.add(name)
 
     def summary(self):
         if not self.samples:

@@ -61,7 +61,10 @@ V3 = MoEConfig("v3", T=4096, d=7168, E=256, n_groups=8, topk_groups=4, K=8, f=20
                n_outlier=72, outlier_scale=30.0, w_std=0.006)
 SKEWED = replace(V3, name="skewed", T=16384, zipf_s=1.1, zipf_beta=0.35)
 DECODE = replace(V3, name="decode", T=128)
-CONFIGS = {c.name: c for c in (TINY, V3, SKEWED, DECODE)}
+# V3 shapes with 32 experts and 512 tokens (about 128 rows per expert, like V3): a small
+# case for profiler captures (1.4 GB of expert weights).
+V3_E32 = replace(V3, name="v3_e32", T=512, E=32)
+CONFIGS = {c.name: c for c in (TINY, V3, SKEWED, DECODE, V3_E32)}
 
 # Standalone FP8 block-scaled GEMM sweep, (M, N, K).
 GEMM_SWEEP = [(4096, 7168, 2048), (4096, 4096, 7168), (8192, 18432, 7168),
