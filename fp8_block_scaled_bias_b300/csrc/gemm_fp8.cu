@@ -274,9 +274,11 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
       if (EPI == kEpiSwiGLU) { nb0 = 2 * nt; nb1 = 2 * nt + 1; }
       else { nb0 = nb1 = 2 * nt + grp; }
       const bool nb_ok = nb1 < NB;
-      float acc[128];
+      // FP32 accumulators as pairs: the promotion runs as packed FP32 FMAs (two lanes'
+      // worth per instruction, each rounded like a single FMA)
+      float2 acc2[64];
 #pragma unroll
-      for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
+      for (int i = 0; i < 64; ++i) acc2[i] = make_float2(0.0f, 0.0f);
       float sa_next = __ldg(sa_col);
       float sb0_next = nb_ok ? __ldg(sb_g + static_cast<long long>(nb0) * KB) : 0.0f;
       float sb1_next = nb_ok ? __ldg(sb_g + static_cast<long long>(nb1) * KB) : 0.0f;
@@ -295,24 +297,30 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
         if (!mbar_wait(tfull_bar(b), bph, abort_flag, p.status)) { ok = false; break; }
         tc_fence_after();
         const uint32_t tb = tmem_base + lane_addr + static_cast<uint32_t>(b * BN);
+        // 16-column chunks keep the staging registers small enough that the 128
+        // accumulators stay in registers (the 10-warp CTA allows 168 per thread)
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 8; ++c) {
           int col;
-          if (EPI == kEpiSwiGLU) col = (c < 2 ? 0 : 128) + grp * 64 + (c & 1) * 32;
-          else col = grp * 128 + c * 32;
-          const float sc = (EPI == kEpiSwiGLU && c >= 2) ? sc1 : sc0;
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tb + static_cast<uint32_t>(col), v);
+          if (EPI == kEpiSwiGLU) col = (c < 4 ? 0 : 128) + grp * 64 + (c & 3) * 16;
+          else col = grp * 128 + c * 16;
+          const float sc = (EPI == kEpiSwiGLU && c >= 4) ? sc1 : sc0;
+          const float2 sc2 = make_float2(sc, sc);
+          uint32_t v[16];
+          tmem_ld_32x32b_x16(tb + static_cast<uint32_t>(col), v);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            acc[c * 32 + i] = __fmaf_rn(sc, __uint_as_float(v[i]), acc[c * 32 + i]);
+          for (int i = 0; i < 8; ++i)
+            acc2[c * 8 + i] = __ffma2_rn(
+                sc2, make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])),
+                acc2[c * 8 + i]);
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(tempty_bar(b));
       }
       if (!ok) break;
+      float* acc = reinterpret_cast<float*>(acc2);
 
       if (EPI == kEpiBF16) {
         const int col0 = nt * BN + grp * 128;

@@ -49,14 +49,19 @@ def test_tiny_weights_quantised_like_oracle(tiny):
         assert np.array_equal(w.s2[e].cpu().numpy(), s2)
 
 
-def _compare_tiny(cfg, layer, ref, x):
+def _compare_tiny(cfg, layer, ref, x, gate_tol=None):
+    """gate_tol None: identical logits on both sides, gates within 16 float32 ulps;
+    else an absolute tolerance (the GPU routed from its own logits)."""
     T, K = cfg.T, cfg.K
     for name in ("idx", "counts", "offsets", "row_token", "row_of", "xq", "sx"):
         got = getattr(layer, name).cpu().numpy()
         assert np.array_equal(got, ref[name]), name
     # from logits the GPU sigmoid uses expf: gates agree to a few float32 ulps
     g = layer.gate.cpu().numpy()
-    assert (np.abs(g - ref["gate"]) <= 16 * 2.0 ** -24 * ref["gate"] + 1e-12).all()
+    if gate_tol is None:
+        assert (np.abs(g - ref["gate"]) <= 16 * 2.0 ** -24 * ref["gate"] + 1e-12).all()
+    else:
+        assert np.abs(g - ref["gate"]).max() <= gate_tol
     # h is requantised from FP32 partial sums: decoded values agree to FP8 rounding
     hq = oracle.dequant_1x128(layer.hq.cpu().numpy(), layer.sh.cpu().numpy())
     hr = oracle.dequant_1x128(ref["hq"], ref["sh"])
@@ -95,7 +100,7 @@ def test_tiny_layer_full_path(tiny):
     z = layer.z.cpu().numpy()
     assert np.abs(z - ref["z"]).max() <= 1e-4 * np.abs(ref["z"]).max()
     if np.array_equal(layer.idx.cpu().numpy(), ref["idx"]):
-        _compare_tiny(cfg, layer, ref, x)
+        _compare_tiny(cfg, layer, ref, x, gate_tol=5e-4)
     else:                                     # a near-tie flipped: compare unaffected tokens
         same = (layer.idx.cpu().numpy() == ref["idx"]).all(1)
         assert same.mean() > 0.99
@@ -165,6 +170,8 @@ def _pool():
         import multiprocessing as mp
         _POOL = cf.ProcessPoolExecutor(max_workers=max(1, min(24, (os.cpu_count() or 2) - 1)),
                                        mp_context=mp.get_context("spawn"))
+        import atexit
+        atexit.register(_POOL.shutdown)
     return _POOL
 
 
