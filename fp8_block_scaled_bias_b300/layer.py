@@ -9,7 +9,7 @@ as one more segment), and the gate-weighted BF16 combine.  The layer output excl
 the residual; ``forward(..., residual=True)`` adds x afterwards.
 
 Weights are prepared once (not timed): expert matrices are quantised 128x128 on the
-GPU and the gate/up matrices are interleaved in 128-row blocks so one 256-column GEMM
+GPU and the gate/up matrices are interleaved in 64-row blocks so one 128-column GEMM
 tile holds matching gate and up columns.
 """
 
@@ -25,16 +25,21 @@ class MoEWeights:
     centroids: torch.Tensor   # FP32 [E, d]
     w_hilo: torch.Tensor      # BF16 [2, E, d]
     bias: torch.Tensor        # FP32 [E]
-    w13: torch.Tensor         # E4M3 [E+1, 2f, d], gate/up interleaved in 128-row blocks
+    w13: torch.Tensor         # E4M3 [E+1, 2f, d], gate/up interleaved in 64-row blocks
     s13: torch.Tensor         # FP32 [E+1, 2f/128, d/128]
     w2: torch.Tensor          # E4M3 [E+1, d, f]
     s2: torch.Tensor          # FP32 [E+1, d/128, f/128]
 
 
 def interleave_gate_up(q1, s1, q3, s3):
-    """Gate [f, d] and up [f, d] codes/scales -> [2f, d] with alternating 128-row blocks."""
+    """Gate [f, d] and up [f, d] codes/scales -> the layout the gate/up GEMM takes.
+
+    Codes alternate in 64-row blocks (rows [128j, 128j+64) = gate rows [64j, 64j+64),
+    rows [128j+64, 128j+128) = the matching up rows), so every 128-column GEMM tile holds
+    matching gate and up columns.  Scales stay per 128x128 block of the original
+    matrices, alternating gate block i, up block i."""
     f, d = q1.shape
-    w13 = torch.stack([q1.view(f // 128, 128, d), q3.view(f // 128, 128, d)], dim=1)
+    w13 = torch.stack([q1.view(f // 64, 64, d), q3.view(f // 64, 64, d)], dim=1)
     s13 = torch.stack([s1, s3], dim=1)
     return w13.reshape(2 * f, d), s13.reshape(2 * f // 128, d // 128)
 

@@ -173,9 +173,11 @@ size_t fp8_grouped_gemm_ws_bytes(int M, int K, int has_a_rows);
  *   [G | U] = xq_rows . w13_e^T   (grouped block-scaled GEMM, FP32 results)
  *   h = silu(G) * U               (FP32), requantised 1x128 along f -> hq, sh
  *   y_rows = hq . w2_e^T          (grouped block-scaled GEMM, BF16 results)
- * w13 interleaves the gate and up weights in 128-row blocks: rows [256j, 256j+128) of
- * expert e are gate rows [128j, 128j+128) and rows [256j+128, 256j+256) the matching up
- * rows, so every 256-column output tile holds matching gate and up columns.
+ * w13 interleaves the gate and up weights in 64-row blocks: rows [128j, 128j+64) of
+ * expert e are gate rows [64j, 64j+64) and rows [128j+64, 128j+128) the matching up
+ * rows, so every 128-column output tile holds matching gate and up columns.  The
+ * scales stay per 128x128 block of the original matrices: s13[e][2i][kb] belongs to
+ * gate rows [128i, 128i+128), s13[e][2i+1][kb] to the same up rows.
  *   xq: uint8 [T][d]; sx: FP32 [d/128][T]; row_token: int32 [rows]; offsets: int32
  *   [n_segments+1] (device), offsets[n_segments] <= rows;
  *   w13: uint8 [n_segments][2f][d]; s13: FP32 [n_segments][2f/128][d/128];
