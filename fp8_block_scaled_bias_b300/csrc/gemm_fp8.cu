@@ -12,11 +12,16 @@
 // into one of four TMEM buffers while the epilogue warps fold finished ones into FP32
 // registers, so the MMAs can run up to three K blocks ahead of the promotion.
 //
-// Kernel shape (one CTA per SM, persistent):
+// Kernel shape (one CTA per SM, persistent, in clusters of cs = 1, 2 or 4 CTAs):
 //   warp 0      TMA producer: A tile 128x128 and B tile 128x128 (FP8) per K block,
-//               6 stages (5 with the SwiGLU epilogue)
+//               6 stages (5 with the SwiGLU epilogue).  The cs CTAs of a cluster work
+//               on neighbouring N tiles of the same row block, so they need the same A
+//               tile: each loads 128/cs of its rows and multicasts them to all, which
+//               divides the A traffic from L2 by cs.
 //   warp 1      TMEM allocation; one thread issues 4 MMAs (M128 N128 K32) per K block
-//               into TMEM buffer (kb mod 4) and commits to the stage / buffer barriers
+//               into TMEM buffer (kb mod 4) and commits to the buffer barrier and to the
+//               stage barrier of every CTA of the cluster (a stage is refilled only when
+//               all cs CTAs have consumed it)
 //   warps 2..9  promotion + epilogue: warp w reads TMEM lanes 32*(w%4).. (its rows);
 //               warps 2-5 own 64 of the 128 columns, warps 6-9 the other 64.  Each
 //               thread issues all four of its 16-column TMEM loads before one wait,
@@ -90,8 +95,8 @@ namespace {
 
 MOE_DEV float silu_f32(float g) { return __fdiv_rn(g, 1.0f + expf(-g)); }
 
-// Work unit -> (segment, first row, valid rows, unit index within the row block).
-// ustart[g] = first unit of segment g (non-decreasing); the largest g with
+// Cluster work unit -> (segment, first row, valid rows, unit index within the row
+// block).  ustart[g] = first unit of segment g (non-decreasing); the largest g with
 // ustart[g] <= unit is non-empty.  Units of a segment run M blocks fastest.
 MOE_DEV void decode_unit(int unit, const int* ustart, const int* seg, int G, int& g, int& m0,
                          int& rows_valid, int& nu) {
@@ -158,8 +163,12 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = p.G;
   const int NT = p.N / BN;                 // N tiles
-  const int NU = NT / TPU;                 // work units per M block
+  const int cs = static_cast<int>(cluster_nctarank());
+  const int crank = static_cast<int>(cluster_ctarank());
+  const int NU = NT / TPU / cs;            // cluster work units per M block
   const int KB = p.K / BK;
+  const uint16_t cmask = static_cast<uint16_t>((1u << cs) - 1u);
+  const int a_rows = BM / cs;              // A rows this CTA loads and multicasts
 
   // ---- segment table and unit prefix (every CTA computes its own copy) ----
   if (tid == 0) { *abort_flag = 0; *bad = 0; }
@@ -207,7 +216,7 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
   const int total = *total_units;
 
   if (tid == 0) {
-    for (int s = 0; s < STAGES; ++s) { mbar_init(full_bar(s), 1); mbar_init(empty_bar(s), 1); }
+    for (int s = 0; s < STAGES; ++s) { mbar_init(full_bar(s), 1); mbar_init(empty_bar(s), cs); }
     for (int b = 0; b < TBUF; ++b) { mbar_init(tfull_bar(b), 1); mbar_init(tempty_bar(b), EPI_WARPS); }
     for (int b = 0; b < 2; ++b) mbar_init(amax_bar(b), EPI_THREADS);
     mbar_init(drain_bar, 1);
@@ -217,26 +226,34 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();          // every CTA's barriers exist before any multicast reaches it
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  const int first_unit = static_cast<int>(cluster_id_x());
+  const int unit_stride = static_cast<int>(ncluster_x());
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
-      for (int unit = blockIdx.x; ok && unit < total; unit += gridDim.x) {
-        int g, m0, rv, nu;
-        decode_unit(unit, ustart, seg, G, g, m0, rv, nu);
+      for (int unit = first_unit; ok && unit < total; unit += unit_stride) {
+        int g, m0, rv, cu;
+        decode_unit(unit, ustart, seg, G, g, m0, rv, cu);
+        const int nu = cu * cs + crank;
         for (int t = 0; ok && t < TPU; ++t) {
           const int brow = g * p.N + (nu * TPU + t) * BN;
           for (int kb = 0; kb < KB; ++kb, ++it) {
             const int s = it % STAGES;
             const uint32_t ph = (it / STAGES) & 1;
             if (!mbar_wait(empty_bar(s), ph ^ 1, abort_flag, p.status)) { ok = false; break; }
-            mbar_arrive_expect_tx(full_bar(s), STAGE_BYTES);
-            tma_load_2d(sbase + L::OFF_A + s * A_BYTES, &tmA, kb * BK, m0, full_bar(s));
+            mbar_arrive_expect_tx(full_bar(s), STAGE_BYTES);   // whole A tile + own B tile
+            const uint32_t a_dst = sbase + L::OFF_A + s * A_BYTES;
+            if (cs == 1)
+              tma_load_2d(a_dst, &tmA, kb * BK, m0, full_bar(s));
+            else
+              tma_load_2d_multicast(a_dst + crank * a_rows * BK, &tmA, kb * BK,
+                                    m0 + crank * a_rows, full_bar(s), cmask);
             tma_load_2d(sbase + L::OFF_B + s * B_BYTES, &tmB, kb * BK, brow, full_bar(s));
           }
         }
@@ -253,7 +270,7 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
       constexpr uint32_t idesc = make_idesc(BM, BN, 0u, 0u);   // E4M3 x E4M3 -> F32
       uint32_t it = 0;
       bool ok = true;
-      for (int unit = blockIdx.x; ok && unit < total; unit += gridDim.x) {
+      for (int unit = first_unit; ok && unit < total; unit += unit_stride) {
         for (int t = 0; ok && t < TPU; ++t) {
           for (int kb = 0; kb < KB; ++kb, ++it) {
             const int s = it % STAGES;
@@ -269,7 +286,8 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
 #pragma unroll
             for (int k = 0; k < BK / 32; ++k)   // K = 32 bytes per MMA: +2 in the >>4 address
               mma_f8f6f4(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, k > 0 ? 1u : 0u);
-            mma_commit(empty_bar(s));
+            if (cs == 1) mma_commit(empty_bar(s));
+            else mma_commit_multicast(empty_bar(s), cmask);
             mma_commit(tfull_bar(b));
           }
         }
@@ -295,9 +313,10 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
     uint32_t it = 0;
     int ucount = 0;
     bool ok = true;
-    for (int unit = blockIdx.x; ok && unit < total; unit += gridDim.x, ++ucount) {
-      int g, m0, rv, nu;
-      decode_unit(unit, ustart, seg, G, g, m0, rv, nu);
+    for (int unit = first_unit; ok && unit < total; unit += unit_stride, ++ucount) {
+      int g, m0, rv, cu;
+      decode_unit(unit, ustart, seg, G, g, m0, rv, cu);
+      const int nu = cu * cs + crank;
       const int arow = min(m0 + row, p.M - 1);
       const float* sa_col = p.sA + arow;
       float amax0 = 0.0f;
@@ -411,7 +430,7 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();          // no CTA leaves while a cluster peer may still write into it
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
@@ -424,12 +443,64 @@ bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* ptr
                     uint64_t inner, uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
                     uint32_t box_outer);   // runtime.cu
 
+namespace {
+
+// Largest cluster size in {4, 2, 1} that divides the work units of one row block.
+int pick_cluster(int units_per_block) {
+  for (int c = 4; c > 1; c >>= 1)
+    if (units_per_block % c == 0) return c;
+  return 1;
+}
+
+template <int EPI>
+int launch_gemm_kernel(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p,
+                       int cs, long long max_units, cudaStream_t stream) {
+  constexpr int smem = gk::Layout<EPI>::SMEM_ALLOC;
+  auto kern = fp8_gemm_kernel<EPI>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+      return MOE_ERR_CUDA;
+    attr_set = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(gk::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // as many clusters as can be resident at once (the kernel is persistent)
+  static int max_clusters[5] = {0, 0, 0, 0, 0};
+  if (max_clusters[cs] == 0) {
+    cfg.gridDim = dim3(static_cast<unsigned>(num_sms() / cs * cs), 1, 1);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) n = num_sms() / cs;
+    max_clusters[cs] = n;
+  }
+  long long clusters = max_clusters[cs];
+  if (max_units < clusters) clusters = max_units;
+  if (clusters < 1) clusters = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(clusters * cs), 1, 1);
+  if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p) != cudaSuccess) return MOE_ERR_CUDA;
+  return check_launch();
+}
+
+}  // namespace
+
 int launch_fp8_gemm(const GemmArgs& a, GemmEpilogue epi, cudaStream_t stream) {
   using namespace gk;
   if (a.M == 0) return MOE_OK;
   if (a.N % BN != 0 || (epi == kEpiSwiGLU && a.N % 256 != 0)) return MOE_ERR_UNSUPPORTED;
+  const int units = a.N / BN / (epi == kEpiSwiGLU ? 2 : 1);     // CTA units per row block
+  const int cs = pick_cluster(units);
   CUtensorMap tmA, tmB;
-  if (!encode_tmap_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.A, a.K, a.M, a.K, BK, BM))
+  if (!encode_tmap_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.A, a.K, a.M, a.K, BK, BM / cs))
     return MOE_ERR_CUDA;
   if (!encode_tmap_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.B,
                       a.K, static_cast<uint64_t>(a.G) * a.N, a.K, BK, BN))
@@ -438,27 +509,9 @@ int launch_fp8_gemm(const GemmArgs& a, GemmEpilogue epi, cudaStream_t stream) {
   p.sA = a.sA; p.sB = a.sB; p.seg = a.seg;
   p.G = a.G; p.M = a.M; p.N = a.N; p.K = a.K;
   p.C = a.C; p.ldc = a.ldc; p.hq = a.hq; p.sh = a.sh; p.status = a.status;
-
-  const int NU = a.N / BN / (epi == kEpiSwiGLU ? 2 : 1);
-  const long long max_units = (static_cast<long long>(a.M) / BM + a.G) * NU;
-  int grid = num_sms();
-  if (max_units < grid) grid = static_cast<int>(max_units);
-  if (grid < 1) grid = 1;
-
-  if (epi == kEpiSwiGLU) {
-    constexpr int smem = Layout<kEpiSwiGLU>::SMEM_ALLOC;
-    if (cudaFuncSetAttribute(fp8_gemm_kernel<kEpiSwiGLU>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-      return MOE_ERR_CUDA;
-    fp8_gemm_kernel<kEpiSwiGLU><<<grid, THREADS, smem, stream>>>(tmA, tmB, p);
-  } else {
-    constexpr int smem = Layout<kEpiBF16>::SMEM_ALLOC;
-    if (cudaFuncSetAttribute(fp8_gemm_kernel<kEpiBF16>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-      return MOE_ERR_CUDA;
-    fp8_gemm_kernel<kEpiBF16><<<grid, THREADS, smem, stream>>>(tmA, tmB, p);
-  }
-  return check_launch();
+  const long long max_units = (static_cast<long long>(a.M) / BM + a.G) * (units / cs);
+  if (epi == kEpiSwiGLU) return launch_gemm_kernel<kEpiSwiGLU>(tmA, tmB, p, cs, max_units, stream);
+  return launch_gemm_kernel<kEpiBF16>(tmA, tmB, p, cs, max_units, stream);
 }
 
 }  // namespace moe
