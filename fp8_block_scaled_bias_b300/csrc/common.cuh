@@ -88,6 +88,15 @@ MOE_DEV bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, int32
   }
 }
 
+// Warp-wide wait: lane 0 polls the barrier (the other lanes do not compete for shared
+// memory while they wait), then the warp resynchronises.  All lanes get the result.
+MOE_DEV bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort, int32_t* status) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort, status) ? 1 : 0;
+  ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+  return ok != 0;
+}
+
 // ---- TMA -----------------------------------------------------------------------------
 
 MOE_DEV void tma_prefetch_desc(const void* tmap) {
@@ -287,9 +296,21 @@ MOE_DEV void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// Named barrier over `nthreads` threads (id 1..15; 0 is __syncthreads).
-MOE_DEV void named_bar_sync(int id, int nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+// Named barrier over `nthreads` threads (id 1..15; 0 is __syncthreads), whole warps,
+// returning the OR of every participating thread's `v`.  A hardware barrier: it does not
+// touch shared memory.  It cannot time out, so the participants must execute it the same
+// number of times by construction.
+MOE_DEV bool named_bar_sync_or(int id, int nthreads, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, %2, %3, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
 }
 
 // ---- number formats ------------------------------------------------------------------

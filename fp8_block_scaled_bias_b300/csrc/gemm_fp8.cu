@@ -21,7 +21,13 @@
 //   warp 1      TMEM allocation; one thread issues 4 MMAs (M128 N128 K32) per K block
 //               into TMEM buffer (kb mod 4) and commits to the buffer barrier and to the
 //               stage barrier of every CTA of the cluster (a stage is refilled only when
-//               all cs CTAs have consumed it)
+//               all cs CTAs have consumed it).  This warp never touches shared memory in
+//               its loop: on this tensor core a shared-memory access by the issuing warp
+//               (an mbarrier wait included) waits behind the operand reads of its MMAs in
+//               flight and leaves the pipe idle.
+//   warp 10     MMA scheduler: waits on the stage and TMEM-buffer mbarriers for each K
+//               block and releases warp 1 through a named barrier (lockstep; its OR-
+//               reduction carries an abort, so both warps leave the loop together)
 //   warps 2..9  promotion + epilogue: warp w reads TMEM lanes 32*(w%4).. (its rows);
 //               warps 2-5 own 64 of the 128 columns, warps 6-9 the other 64.  Each
 //               thread issues all four of its 16-column TMEM loads before one wait,
@@ -54,7 +60,9 @@ constexpr int B_BYTES = BN * BK;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int EPI_WARPS = 8;
 constexpr int EPI_THREADS = EPI_WARPS * 32;
-constexpr int THREADS = 64 + EPI_THREADS;
+constexpr int SCHED_WARP = 2 + EPI_WARPS;          // waits on barriers for the MMA warp
+constexpr int THREADS = 64 + EPI_THREADS + 32;
+constexpr int MMA_BAR = 1;                         // named barrier: MMA warp + scheduler
 constexpr int MAX_G = 1024;
 constexpr int TBUF = 4;                  // TMEM partial buffers of BN columns
 constexpr uint32_t TMEM_COLS = 512;
@@ -265,20 +273,18 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
       }
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0) {
-      constexpr uint32_t idesc = make_idesc(BM, BN, 0u, 0u);   // E4M3 x E4M3 -> F32
-      uint32_t it = 0;
-      bool ok = true;
-      for (int unit = first_unit; ok && unit < total; unit += unit_stride) {
-        for (int t = 0; ok && t < TPU; ++t) {
-          for (int kb = 0; kb < KB; ++kb, ++it) {
+    // ---------------- MMA issuer (no shared-memory access in the loop) ----------------
+    constexpr uint32_t idesc = make_idesc(BM, BN, 0u, 0u);   // E4M3 x E4M3 -> F32
+    uint32_t it = 0;
+    bool ok = true;
+    for (int unit = first_unit; ok && unit < total; unit += unit_stride) {
+      for (int t = 0; ok && t < TPU; ++t) {
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          // released by the scheduler once stage s is full and TMEM buffer b is free
+          if (named_bar_sync_or(MMA_BAR, 64, false)) { ok = false; break; }
+          if (lane == 0) {
             const int s = it % STAGES;
-            const uint32_t ph = (it / STAGES) & 1;
             const int b = it % TBUF;
-            const uint32_t bph = (it / TBUF) & 1;
-            if (!mbar_wait(tempty_bar(b), bph ^ 1, abort_flag, p.status)) { ok = false; break; }
-            if (!mbar_wait(full_bar(s), ph, abort_flag, p.status)) { ok = false; break; }
             tc_fence_after();
             const uint64_t adesc = smem_desc_sw128(sbase + L::OFF_A + s * A_BYTES);
             const uint64_t bdesc = smem_desc_sw128(sbase + L::OFF_B + s * B_BYTES);
@@ -290,13 +296,40 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
             else mma_commit_multicast(empty_bar(s), cmask);
             mma_commit(tfull_bar(b));
           }
+          __syncwarp();
         }
       }
-      // every MMA issued so far must finish before TMEM is released
+    }
+    // every MMA issued so far must finish before TMEM is released
+    if (lane == 0) {
       mma_commit(drain_bar);
       mbar_drain(drain_bar, 0);
     }
-  } else {
+    __syncwarp();
+  } else if (warp == SCHED_WARP) {
+    // ---------------- MMA scheduler ----------------
+    // Same iteration sequence as the MMA warp; one named barrier per K block.
+    uint32_t it = 0;
+    bool ok = true;
+    for (int unit = first_unit; ok && unit < total; unit += unit_stride) {
+      for (int t = 0; ok && t < TPU; ++t) {
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          int good = 1;
+          if (lane == 0) {
+            const int s = it % STAGES;
+            const uint32_t ph = (it / STAGES) & 1;
+            const int b = it % TBUF;
+            const uint32_t bph = (it / TBUF) & 1;
+            good = mbar_wait(tempty_bar(b), bph ^ 1, abort_flag, p.status) &&
+                   mbar_wait(full_bar(s), ph, abort_flag, p.status);
+          }
+          good = __shfl_sync(0xFFFFFFFFu, good, 0);
+          tc_fence_before();
+          if (named_bar_sync_or(MMA_BAR, 64, good == 0)) { ok = false; break; }
+        }
+      }
+    }
+  } else if (warp >= 2 && warp < 2 + EPI_WARPS) {
     // ---------------- promotion + epilogue ----------------
     const int etid = tid - 64;
     const int grp = (warp - 2) >> 2;    // column half of the tile
@@ -342,7 +375,7 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
           const float sc0 = __fmul_rn(sa, sb0), sc1 = __fmul_rn(sa, sb1);
           const int b = it % TBUF;
           const uint32_t bph = (it / TBUF) & 1;
-          if (!mbar_wait(tfull_bar(b), bph, abort_flag, p.status)) { ok = false; break; }
+          if (!mbar_wait_warp(tfull_bar(b), bph, abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
           const uint32_t tb = tmem_base + lane_addr + static_cast<uint32_t>(b * BN);
           uint32_t v[4][16];
@@ -399,7 +432,7 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
           const int buf = ucount & 1;
           amax_x[(buf * 2 + grp) * BM + row] = amax;
           mbar_arrive(amax_bar(buf));
-          if (!mbar_wait(amax_bar(buf), (ucount >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
+          if (!mbar_wait_warp(amax_bar(buf), (ucount >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
           amax = fmaxf(amax, amax_x[(buf * 2 + (grp ^ 1)) * BM + row]);
           const float s = e4m3_scale_from_amax(amax);
           if (row < rv) {
@@ -447,8 +480,10 @@ namespace {
 
 // Largest cluster size in {4, 2, 1} that divides the work units of one row block.
 int pick_cluster(int units_per_block) {
-  for (int c = 4; c > 1; c >>= 1)
-    if (units_per_block % c == 0) return c;
+  // Clusters share the A tile through multicast, which cuts L2 traffic but not the
+  // shared-memory traffic that bounds this kernel, and 4-CTA clusters leave SMs idle
+  // (fewer can be resident at once); one-CTA clusters measured faster.
+  (void)units_per_block;
   return 1;
 }
 
