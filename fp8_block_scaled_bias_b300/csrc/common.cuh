@@ -134,6 +134,18 @@ MOE_DEV void tma_load_2d_multicast(uint32_t dst, const void* tmap, int32_t x, in
       : "memory");
 }
 
+// ---- cp.async (per-thread asynchronous global -> shared copies) ----------------------------
+
+MOE_DEV void cp_async_4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+
+MOE_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+// Wait until at most N of this thread's committed groups are still in flight.
+template <int N>
+MOE_DEV void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
 // ---- thread-block clusters -------------------------------------------------------------
 
 MOE_DEV uint32_t cluster_ctarank() {

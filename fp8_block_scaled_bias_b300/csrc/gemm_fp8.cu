@@ -63,6 +63,7 @@ constexpr int EPI_THREADS = EPI_WARPS * 32;
 constexpr int SCHED_WARP = 2 + EPI_WARPS;          // waits on barriers for the MMA warp
 constexpr int THREADS = 64 + EPI_THREADS + 32;
 constexpr int MMA_BAR = 1;                         // named barrier: MMA warp + scheduler
+constexpr int SPF = 8;                             // K blocks of scales prefetched ahead
 constexpr int MAX_G = 1024;
 constexpr int TBUF = 4;                  // TMEM partial buffers of BN columns
 constexpr uint32_t TMEM_COLS = 512;
@@ -81,7 +82,10 @@ struct Layout {
   static constexpr int OFF_SEG = OFF_MISC + 16;
   static constexpr int OFF_TSTART = OFF_SEG + (MAX_G + 1) * 4;
   static constexpr int OFF_AMAX = OFF_TSTART + (MAX_G + 1) * 4;   // [2 bufs][2 groups][128]
-  static constexpr int SMEM_USED = OFF_AMAX + 2 * 2 * BM * 4;
+  // per-thread rings of prefetched scales: sA [SPF][EPI_THREADS], sB [SPF][EPI_WARPS][2]
+  static constexpr int OFF_SCALE_A = OFF_AMAX + 2 * 2 * BM * 4;
+  static constexpr int OFF_SCALE_B = OFF_SCALE_A + SPF * EPI_THREADS * 4;
+  static constexpr int SMEM_USED = OFF_SCALE_B + SPF * EPI_WARPS * 2 * 4;
   static constexpr int SMEM_ALLOC = SMEM_USED + 1024;              // 1024-B alignment slack
   static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 };
@@ -343,6 +347,57 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
     for (int c = 0; c < 4; ++c)
       cols[c] = (EPI == kEpiSwiGLU) ? (c < 2 ? 0 : 64) + grp * 32 + (c & 1) * 16
                                     : grp * 64 + c * 16;
+    // Scale prefetch: every K block needs sA[kb][row] (this thread's row) and the one or
+    // two weight scales of the tile's N blocks.  They are copied into shared-memory rings
+    // SPF K blocks ahead with cp.async, following the same (unit, tile, K block) sequence
+    // as the promotion loop, so the L2 latency never sits on the critical path.
+    const uint32_t ring_a = sbase + L::OFF_SCALE_A + static_cast<uint32_t>(etid) * 4;
+    const uint32_t ring_b = sbase + L::OFF_SCALE_B + static_cast<uint32_t>(warp - 2) * 8;
+    const float* ring_a_f = reinterpret_cast<const float*>(smem + L::OFF_SCALE_A) + etid;
+    const float* ring_b_f = reinterpret_cast<const float*>(smem + L::OFF_SCALE_B) + (warp - 2) * 2;
+    int pf_unit = first_unit, pf_t = 0, pf_kb = 0;       // prefetch cursor
+    int pf_g = 0, pf_m0 = 0, pf_nu = 0;
+    bool pf_live = pf_unit < total;
+    if (pf_live) {
+      int rv_unused, cu;
+      decode_unit(pf_unit, ustart, seg, G, pf_g, pf_m0, rv_unused, cu);
+      pf_nu = cu * cs + crank;
+    }
+    uint32_t pf_it = 0;
+    auto prefetch_one = [&]() {
+      // issue the copies of the cursor's K block into ring slot pf_it % SPF, then advance
+      if (pf_live) {
+        const int nt = pf_nu * TPU + pf_t;
+        const int nb0 = (EPI == kEpiSwiGLU) ? 2 * (nt >> 1) : nt;
+        const int nb1 = (EPI == kEpiSwiGLU) ? nb0 + 1 : nt;
+        const int slot = static_cast<int>(pf_it % SPF);
+        const int arow = min(pf_m0 + row, p.M - 1);
+        cp_async_4(ring_a + slot * EPI_THREADS * 4,
+                   p.sA + static_cast<long long>(pf_kb) * p.M + arow);
+        if (lane == 0) {
+          const float* sb = p.sB + static_cast<long long>(pf_g) * NB * KB + pf_kb;
+          cp_async_4(ring_b + slot * EPI_WARPS * 8, sb + static_cast<long long>(nb0) * KB);
+          cp_async_4(ring_b + slot * EPI_WARPS * 8 + 4, sb + static_cast<long long>(nb1) * KB);
+        }
+        if (++pf_kb == KB) {
+          pf_kb = 0;
+          if (++pf_t == TPU) {
+            pf_t = 0;
+            pf_unit += unit_stride;
+            pf_live = pf_unit < total;
+            if (pf_live) {
+              int rv_unused, cu;
+              decode_unit(pf_unit, ustart, seg, G, pf_g, pf_m0, rv_unused, cu);
+              pf_nu = cu * cs + crank;
+            }
+          }
+        }
+      }
+      cp_async_commit();                                 // one group per K block, maybe empty
+      ++pf_it;
+    };
+    for (int i = 0; i < SPF - 1; ++i) prefetch_one();
+
     uint32_t it = 0;
     int ucount = 0;
     bool ok = true;
@@ -350,29 +405,21 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
       int g, m0, rv, cu;
       decode_unit(unit, ustart, seg, G, g, m0, rv, cu);
       const int nu = cu * cs + crank;
-      const int arow = min(m0 + row, p.M - 1);
-      const float* sa_col = p.sA + arow;
+      (void)g;
       float amax0 = 0.0f;
       for (int t = 0; ok && t < TPU; ++t) {
         const int nt = nu * TPU + t;
-        // weight-scale rows of this thread's columns (gate and up blocks for SwiGLU)
-        const int nb0 = (EPI == kEpiSwiGLU) ? 2 * (nt >> 1) : nt;
-        const int nb1 = (EPI == kEpiSwiGLU) ? nb0 + 1 : nt;
-        const float* sb0p = p.sB + (static_cast<long long>(g) * NB + nb0) * KB;
-        const float* sb1p = p.sB + (static_cast<long long>(g) * NB + nb1) * KB;
         float2 acc2[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) acc2[i] = make_float2(0.0f, 0.0f);
-        float sa_next = __ldg(sa_col);
-        float sb0_next = __ldg(sb0p), sb1_next = __ldg(sb1p);
         for (int kb = 0; kb < KB; ++kb, ++it) {
-          const float sa = sa_next, sb0 = sb0_next, sb1 = sb1_next;
-          if (kb + 1 < KB) {
-            sa_next = __ldg(sa_col + static_cast<long long>(kb + 1) * p.M);
-            sb0_next = __ldg(sb0p + kb + 1);
-            sb1_next = __ldg(sb1p + kb + 1);
-          }
-          const float sc0 = __fmul_rn(sa, sb0), sc1 = __fmul_rn(sa, sb1);
+          prefetch_one();                                // K block it + SPF - 1
+          cp_async_wait<SPF - 1>();                      // this thread's copies for `it` landed
+          __syncwarp();                                  // lane 0's weight scales too
+          const int slot = static_cast<int>(it % SPF);
+          const float sa = ring_a_f[slot * EPI_THREADS];
+          const float sc0 = __fmul_rn(sa, ring_b_f[slot * EPI_WARPS * 2]);
+          const float sc1 = __fmul_rn(sa, ring_b_f[slot * EPI_WARPS * 2 + 1]);
           const int b = it % TBUF;
           const uint32_t bph = (it / TBUF) & 1;
           if (!mbar_wait_warp(tfull_bar(b), bph, abort_flag, p.status)) { ok = false; break; }
@@ -460,6 +507,7 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
         }
       }
     }
+    cp_async_wait<0>();                                  // no copy may land after exit
   }
 
   tc_fence_before();
