@@ -9,17 +9,17 @@
 // that interval ("DeepSeek-V3" summary, core idea 6(b); book ch. 16 "Periodic
 // high-precision promotion").  The pages did this on Hopper with two warpgroups taking
 // turns on register accumulators; here the tensor core writes each K block's partial
-// into one of four TMEM buffers while the epilogue warps fold finished ones into FP32
-// registers, so the MMAs can run up to three K blocks ahead of the promotion.
+// into one of two TMEM buffers while the epilogue warps fold the other into FP32
+// registers.
 //
 // Kernel shape (one CTA per SM, persistent, in clusters of cs = 1, 2 or 4 CTAs):
-//   warp 0      TMA producer: A tile 128x128 and B tile 128x128 (FP8) per K block,
-//               6 stages (5 with the SwiGLU epilogue).  The cs CTAs of a cluster work
+//   warp 0      TMA producer: A tile 128x128 and B tile 256x128 (FP8) per K block,
+//               4 stages.  The cs CTAs of a cluster work
 //               on neighbouring N tiles of the same row block, so they need the same A
 //               tile: each loads 128/cs of its rows and multicasts them to all, which
 //               divides the A traffic from L2 by cs.
-//   warp 1      TMEM allocation; one thread issues 4 MMAs (M128 N128 K32) per K block
-//               into TMEM buffer (kb mod 4) and commits to the buffer barrier and to the
+//   warp 1      TMEM allocation; one thread issues 4 MMAs (M128 N256 K32) per K block
+//               into TMEM buffer (kb mod 2) and commits to the buffer barrier and to the
 //               stage barrier of every CTA of the cluster (a stage is refilled only when
 //               all cs CTAs have consumed it).  This warp never touches shared memory in
 //               its loop: on this tensor core a shared-memory access by the issuing warp
@@ -29,10 +29,11 @@
 //               block and releases warp 1 through a named barrier (lockstep; its OR-
 //               reduction carries an abort, so both warps leave the loop together)
 //   warps 2..9  promotion + epilogue: warp w reads TMEM lanes 32*(w%4).. (its rows);
-//               warps 2-5 own 64 of the 128 columns, warps 6-9 the other 64.  Each
-//               thread issues all four of its 16-column TMEM loads before one wait,
-//               then adds them into 64 FP32 accumulators with packed FMAs.
-// Tiles are 128 rows x 128 columns.  The tile list walks segments in order, then N
+//               warps 2-5 own 128 of the 256 columns, warps 6-9 the other 128.  Each
+//               thread adds its partials into 128 FP32 accumulators with packed FMAs,
+//               16 columns per TMEM load; the scales arrive through cp.async rings.
+// Tiles are 128 rows x 256 columns; the per-K-block synchronisation costs about the
+// same for any tile width, so the wider tile amortises it over twice the MMA work.  The tile list walks segments in order, then N
 // tiles, with the M tiles of a segment fastest so CTAs working at the same time share
 // the expert's weight tile through L2.  Segments need not be multiples of 128 rows:
 // rows past a segment's end are computed and not stored.
@@ -40,12 +41,11 @@
 // Epilogues:
 //   kEpiBF16    C = BF16(acc)
 //   kEpiSwiGLU  B rows [128j, 128j+64) are gate rows [64j, 64j+64) and rows
-//               [128j+64, 128j+128) the matching up rows, so each thread holds 32 gate
-//               and the 32 matching up accumulators of its row: h = silu(gate) * up.
-//               One CTA runs N tiles 2p and 2p+1 back to back; they cover hidden
-//               columns [128p, 128p+128), one 1x128 group, so the first tile's h waits
-//               in shared memory until the second's is known, then both are
-//               requantised with the group's scale -> hq (E4M3) and sh (FP32).
+//               [128j+64, 128j+128) the matching up rows, so N tile p (256 columns)
+//               covers hidden columns [128p, 128p+128), one 1x128 group, and each
+//               thread holds 64 gate and the 64 matching up accumulators of its row:
+//               h = silu(gate) * up.  The two threads of a row exchange their max-abs
+//               through shared memory and requantise h -> hq (E4M3) and sh (FP32).
 #include <cuda.h>
 
 #include "common.cuh"
@@ -54,7 +54,7 @@
 namespace moe {
 
 namespace gk {
-constexpr int BM = 128, BN = 128, BK = 128;
+constexpr int BM = 128, BN = 256, BK = 128;
 constexpr int A_BYTES = BM * BK;
 constexpr int B_BYTES = BN * BK;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -65,13 +65,13 @@ constexpr int THREADS = 64 + EPI_THREADS + 32;
 constexpr int MMA_BAR = 1;                         // named barrier: MMA warp + scheduler
 constexpr int SPF = 8;                             // K blocks of scales prefetched ahead
 constexpr int MAX_G = 1024;
-constexpr int TBUF = 4;                  // TMEM partial buffers of BN columns
+constexpr int TBUF = 2;                  // TMEM partial buffers of BN columns
 constexpr uint32_t TMEM_COLS = 512;
 
 template <int EPI>
 struct Layout {
-  static constexpr int STAGES = EPI == kEpiSwiGLU ? 5 : 6;
-  static constexpr int STASH = EPI == kEpiSwiGLU ? 32 * EPI_THREADS * 4 : 0;   // h of tile 2p
+  static constexpr int STAGES = 4;
+  static constexpr int STASH = 0;
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
   static constexpr int OFF_STASH = OFF_B + STAGES * B_BYTES;
@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
   using namespace gk;
   using L = Layout<EPI>;
   constexpr int STAGES = L::STAGES;
-  constexpr int TPU = EPI == kEpiSwiGLU ? 2 : 1;     // N tiles per work unit
+  constexpr int TPU = 1;                             // N tiles per work unit
   extern __shared__ uint8_t gemm_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(gemm_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -170,11 +170,10 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
   int* seg = reinterpret_cast<int*>(smem + L::OFF_SEG);
   int* ustart = reinterpret_cast<int*>(smem + L::OFF_TSTART);
   float* amax_x = reinterpret_cast<float*>(smem + L::OFF_AMAX);
-  float* stash = reinterpret_cast<float*>(smem + L::OFF_STASH);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = p.G;
-  const int NT = p.N / BN;                 // N tiles
+  const int NT = (p.N + BN - 1) / BN;      // N tiles (the last may be half-filled)
   const int cs = static_cast<int>(cluster_nctarank());
   const int crank = static_cast<int>(cluster_ctarank());
   const int NU = NT / TPU / cs;            // cluster work units per M block
@@ -341,12 +340,12 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
     const int row = q * 32 + lane;      // row within the tile
     const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
     const int NB = p.N / 128;           // weight-scale rows per segment
-    // TMEM columns of this thread's four 16-column chunks
-    int cols[4];
+    // TMEM columns of this thread's eight 16-column chunks (SwiGLU: 4 gate then 4 up)
+    int cols[8];
 #pragma unroll
-    for (int c = 0; c < 4; ++c)
-      cols[c] = (EPI == kEpiSwiGLU) ? (c < 2 ? 0 : 64) + grp * 32 + (c & 1) * 16
-                                    : grp * 64 + c * 16;
+    for (int c = 0; c < 8; ++c)
+      cols[c] = (EPI == kEpiSwiGLU) ? grp * 128 + (c < 4 ? 0 : 64) + (c & 3) * 16
+                                    : grp * 128 + c * 16;
     // Scale prefetch: every K block needs sA[kb][row] (this thread's row) and the one or
     // two weight scales of the tile's N blocks.  They are copied into shared-memory rings
     // SPF K blocks ahead with cp.async, following the same (unit, tile, K block) sequence
@@ -368,8 +367,9 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
       // issue the copies of the cursor's K block into ring slot pf_it % SPF, then advance
       if (pf_live) {
         const int nt = pf_nu * TPU + pf_t;
-        const int nb0 = (EPI == kEpiSwiGLU) ? 2 * (nt >> 1) : nt;
-        const int nb1 = (EPI == kEpiSwiGLU) ? nb0 + 1 : nt;
+        // (a half-filled last tile has no second N block: read a valid scale, unused)
+        const int nb0 = (EPI == kEpiSwiGLU) ? 2 * nt : min(2 * nt + grp, NB - 1);
+        const int nb1 = (EPI == kEpiSwiGLU) ? 2 * nt + 1 : nb0;
         const int slot = static_cast<int>(pf_it % SPF);
         const int arow = min(pf_m0 + row, p.M - 1);
         cp_async_4(ring_a + slot * EPI_THREADS * 4,
@@ -406,12 +406,11 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
       decode_unit(unit, ustart, seg, G, g, m0, rv, cu);
       const int nu = cu * cs + crank;
       (void)g;
-      float amax0 = 0.0f;
       for (int t = 0; ok && t < TPU; ++t) {
         const int nt = nu * TPU + t;
-        float2 acc2[32];
+        float2 acc2[64];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) acc2[i] = make_float2(0.0f, 0.0f);
+        for (int i = 0; i < 64; ++i) acc2[i] = make_float2(0.0f, 0.0f);
         for (int kb = 0; kb < KB; ++kb, ++it) {
           prefetch_one();                                // K block it + SPF - 1
           cp_async_wait<SPF - 1>();                      // this thread's copies for `it` landed
@@ -425,33 +424,32 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
           if (!mbar_wait_warp(tfull_bar(b), bph, abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
           const uint32_t tb = tmem_base + lane_addr + static_cast<uint32_t>(b * BN);
-          uint32_t v[4][16];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x16(tb + static_cast<uint32_t>(cols[c]), v[c]);
-          tmem_ld_wait();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(tempty_bar(b));     // the buffer is in registers now
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const float sc = (c < 2) ? sc0 : sc1;
+          for (int c = 0; c < 8; ++c) {
+            const float sc = (c < 4) ? sc0 : sc1;
             const float2 sc2 = make_float2(sc, sc);
+            uint32_t v[16];
+            tmem_ld_32x32b_x16(tb + static_cast<uint32_t>(cols[c]), v);
+            tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 8; ++i)
               acc2[c * 8 + i] = __ffma2_rn(
-                  sc2, make_float2(__uint_as_float(v[c][2 * i]), __uint_as_float(v[c][2 * i + 1])),
+                  sc2, make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])),
                   acc2[c * 8 + i]);
           }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tempty_bar(b));     // the buffer is folded in
         }
         if (!ok) break;
         float* acc = reinterpret_cast<float*>(acc2);
 
         if (EPI == kEpiBF16) {
-          if (row < rv) {
+          if (row < rv && nt * BN + grp * 128 < p.N) {
             uint4* dst = reinterpret_cast<uint4*>(p.C + static_cast<long long>(m0 + row) * p.ldc +
-                                                  nt * BN + grp * 64);
+                                                  nt * BN + grp * 128);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
+            for (int j = 0; j < 16; ++j) {
               uint4 o;
               o.x = pack_bf16x2(acc[8 * j + 0], acc[8 * j + 1]);
               o.y = pack_bf16x2(acc[8 * j + 2], acc[8 * j + 3]);
@@ -461,21 +459,13 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
             }
           }
         } else {
-          // h = silu(gate) * up for this thread's 32 hidden columns of this tile
+          // h = silu(gate) * up for this thread's 64 hidden columns
           float amax = 0.0f;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            acc[i] = __fmul_rn(silu_f32(acc[i]), acc[32 + i]);
+          for (int i = 0; i < 64; ++i) {
+            acc[i] = __fmul_rn(silu_f32(acc[i]), acc[64 + i]);
             amax = fmaxf(amax, fabsf(acc[i]));
           }
-          if (t == 0) {
-            // first half of the 1x128 group: keep h until the second half is known
-#pragma unroll
-            for (int i = 0; i < 32; ++i) stash[i * EPI_THREADS + etid] = acc[i];
-            amax0 = amax;
-            continue;
-          }
-          amax = fmaxf(amax, amax0);
           const int buf = ucount & 1;
           amax_x[(buf * 2 + grp) * BM + row] = amax;
           mbar_arrive(amax_bar(buf));
@@ -484,25 +474,17 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
           const float s = e4m3_scale_from_amax(amax);
           if (row < rv) {
             const int f = p.N / 2;
-            uint8_t* hrow = p.hq + static_cast<long long>(m0 + row) * f + nu * 128 + grp * 32;
-            uint4* d0 = reinterpret_cast<uint4*>(hrow);           // hidden cols of tile 2p
-            uint4* d1 = reinterpret_cast<uint4*>(hrow + 64);      // hidden cols of tile 2p+1
+            uint4* dst = reinterpret_cast<uint4*>(p.hq + static_cast<long long>(m0 + row) * f +
+                                                  nt * 128 + grp * 64);
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-              float h0[16];
-#pragma unroll
-              for (int i = 0; i < 16; ++i) h0[i] = stash[(16 * j + i) * EPI_THREADS + etid];
-              d0[j] = make_uint4(e4m3x4(h0[0], h0[1], h0[2], h0[3], s),
-                                 e4m3x4(h0[4], h0[5], h0[6], h0[7], s),
-                                 e4m3x4(h0[8], h0[9], h0[10], h0[11], s),
-                                 e4m3x4(h0[12], h0[13], h0[14], h0[15], s));
-              const float* h1 = acc + 16 * j;
-              d1[j] = make_uint4(e4m3x4(h1[0], h1[1], h1[2], h1[3], s),
-                                 e4m3x4(h1[4], h1[5], h1[6], h1[7], s),
-                                 e4m3x4(h1[8], h1[9], h1[10], h1[11], s),
-                                 e4m3x4(h1[12], h1[13], h1[14], h1[15], s));
+            for (int j = 0; j < 4; ++j) {
+              const float* h = acc + 16 * j;
+              dst[j] = make_uint4(e4m3x4(h[0], h[1], h[2], h[3], s),
+                                  e4m3x4(h[4], h[5], h[6], h[7], s),
+                                  e4m3x4(h[8], h[9], h[10], h[11], s),
+                                  e4m3x4(h[12], h[13], h[14], h[15], s));
             }
-            if (grp == 0) p.sh[static_cast<long long>(nu) * p.M + m0 + row] = s;
+            if (grp == 0) p.sh[static_cast<long long>(nt) * p.M + m0 + row] = s;
           }
         }
       }
@@ -579,8 +561,8 @@ int launch_gemm_kernel(const CUtensorMap& tmA, const CUtensorMap& tmB, const Gem
 int launch_fp8_gemm(const GemmArgs& a, GemmEpilogue epi, cudaStream_t stream) {
   using namespace gk;
   if (a.M == 0) return MOE_OK;
-  if (a.N % BN != 0 || (epi == kEpiSwiGLU && a.N % 256 != 0)) return MOE_ERR_UNSUPPORTED;
-  const int units = a.N / BN / (epi == kEpiSwiGLU ? 2 : 1);     // CTA units per row block
+  if (a.N % 128 != 0 || (epi == kEpiSwiGLU && a.N % BN != 0)) return MOE_ERR_UNSUPPORTED;
+  const int units = (a.N + BN - 1) / BN;                        // CTA units per row block
   const int cs = pick_cluster(units);
   CUtensorMap tmA, tmB;
   if (!encode_tmap_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.A, a.K, a.M, a.K, BK, BM / cs))
