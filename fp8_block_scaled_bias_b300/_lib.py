@@ -26,6 +26,7 @@ SIGNATURES = {
     "moe_route": (_I, [_P, _I, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P]),
     "moe_permute": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_permute_ws_bytes": (_SZ, [_I, _I, _I]),
+    "moe_permute_noalloc": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
     "fp8_quant_1x128": (_I, [_P, _I, _I, _I, _P, _P, _P]),
     "fp8_quant_128x128": (_I, [_P, _I, _I, _P, _P, _P]),
     "fp8_blockscaled_grouped_gemm": (_I, [_P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P, _I,

@@ -100,6 +100,23 @@ int moe_permute(const int32_t* topk_idx, int T, int K, int E, int include_shared
                              row_of, dev_status, ws, as_stream(stream));
 }
 
+int moe_permute_noalloc(const int32_t* topk_idx, int T, int K, int E, int include_shared,
+                        int32_t* counts, int32_t* offsets, int32_t* row_token, int32_t* row_of,
+                        int32_t* dev_status, void* stream) {
+  if (T < 0 || K < 1 || E < 1) return MOE_ERR_INVALID_ARG;
+  if (E > 1024 || K > 32) return MOE_ERR_UNSUPPORTED;
+  if (static_cast<long long>(T) * (K + 1) > INT32_MAX) return MOE_ERR_UNSUPPORTED;
+  if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!topk_idx || !row_token || !row_of)) return MOE_ERR_INVALID_ARG;
+  const long long need = static_cast<long long>(moe::permute_ws_bytes(T, K, E) / sizeof(int32_t));
+  if (need > moe::permute_noalloc_max_ints()) return MOE_ERR_UNSUPPORTED;
+  int32_t* scratch = nullptr;
+  const int st = moe::permute_noalloc_scratch(&scratch);
+  if (st != MOE_OK) return st;
+  return moe::launch_permute(topk_idx, T, K, E, include_shared, counts, offsets, row_token,
+                             row_of, dev_status, scratch, as_stream(stream));
+}
+
 // ---- quantisation --------------------------------------------------------------------
 
 int fp8_quant_1x128(const uint16_t* x, int rows, int cols, int ldx, uint8_t* q, float* scale,

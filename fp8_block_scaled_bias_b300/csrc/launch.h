@@ -29,6 +29,11 @@ int launch_permute(const int32_t* idx, int T, int K, int E, int include_shared,
                    int32_t* counts, int32_t* offsets, int32_t* row_token, int32_t* row_of,
                    int32_t* status, void* ws, cudaStream_t stream);
 
+// Allocation-free permutation scratch (permute.cu): capacity in int32 and the device
+// address of the static array on the current device (looked up once per device).
+long long permute_noalloc_max_ints();
+int permute_noalloc_scratch(int32_t** out);
+
 int launch_combine(const uint16_t* y_rows, int n_rows, const int32_t* row_of,
                    const float* gate, int T, int K, int d, int shared_row_base, uint16_t* y,
                    int32_t* status, cudaStream_t stream);

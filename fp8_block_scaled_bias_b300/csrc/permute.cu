@@ -9,6 +9,8 @@
 //   scatter  thread e walks the chunk's pairs in (token, slot) order and hands out rows
 // Every step is integer work in a fixed order, so the result is deterministic and equal
 // to a stable sort whatever the launch timing.
+#include <mutex>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -146,6 +148,41 @@ int launch_permute(const int32_t* idx, int T, int K, int E, int include_shared,
                                                                 chunk, row_token, row_of);
     if (check_launch() != MOE_OK) return MOE_ERR_CUDA;
   }
+  return MOE_OK;
+}
+
+// ---- allocation-free variant -----------------------------------------------------------
+//
+// Scratch for moe_permute_noalloc: the per-chunk expert histograms live in this
+// file-scope device array instead of caller memory.  Every GPU that loads the library
+// holds it (1 MiB) until the process exits.  In host code the name is only a host-side
+// stand-in, so its device address is looked up with cudaGetSymbolAddress, once per
+// device, while that device is current.
+
+constexpr long long kNoAllocScratchInts = 262144;          // 1 MiB of int32
+static __device__ __align__(256) int32_t g_permute_scratch[kNoAllocScratchInts];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+int32_t* g_scratch_ptr[kMaxDevices] = {nullptr};
+}  // namespace
+
+long long permute_noalloc_max_ints() { return kNoAllocScratchInts; }
+
+int permute_noalloc_scratch(int32_t** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_permute_scratch) != cudaSuccess || !ptr) {
+      cudaGetLastError();
+      return MOE_ERR_CUDA;
+    }
+    g_scratch_ptr[dev] = static_cast<int32_t*>(ptr);
+  }
+  *out = g_scratch_ptr[dev];
   return MOE_OK;
 }
 

@@ -127,6 +127,25 @@ int moe_permute(const int32_t* topk_idx, int T, int K, int E, int include_shared
                 int32_t* dev_status, void* ws, size_t ws_bytes, void* stream);
 size_t moe_permute_ws_bytes(int T, int K, int E);
 
+/* moe_permute without caller workspace (the pages have no counterpart: this is a
+ * convenience of this library).  Same arguments, results and errors as moe_permute,
+ * minus (ws, ws_bytes).  For callers that cannot allocate device memory at the point of
+ * the call -- code recorded into a CUDA graph, where cudaMalloc may not be called,
+ * runtimes that own all device memory through their own allocator, or latency-critical
+ * loops where an allocation would synchronise the device.
+ *   - The scratch is a static device array of 1 MiB (262144 int32) inside the library;
+ *     every GPU that loads the library holds it until the process exits.  Calls whose
+ *     scratch need, ceil(T/128) * E int32, exceeds it return MOE_ERR_UNSUPPORTED.
+ *   - The first call on each device looks up the array's device address (with that
+ *     device current); make that first call before any stream capture.
+ *   - Every call shares the one array and nothing in it needs to start at zero (each
+ *     call writes every entry it reads).  Calls that overlap on the GPU, e.g. on two
+ *     streams without ordering between them, race on it: serialise them.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library routine. */
+int moe_permute_noalloc(const int32_t* topk_idx, int T, int K, int E, int include_shared,
+                        int32_t* counts, int32_t* offsets, int32_t* row_token, int32_t* row_of,
+                        int32_t* dev_status, void* stream);
+
 /* ---- FP8 quantisation -------------------------------------------------------------- */
 
 /* Quantise BF16 x [rows][cols] (row pitch ldx elements) to E4M3 with one FP32 scale per

@@ -80,6 +80,8 @@ def test_host_argument_checks_need_no_gpu():
     assert lib.moe_permute(P, 8, 4, 2000, 1, P, P, P, P, None, P, 1 << 20, None) == -2
     assert lib.moe_permute(P, 8, 40, 16, 1, P, P, P, P, None, P, 1 << 20, None) == -2
     assert lib.moe_permute(P, 8, 4, 16, 1, P, P, P, P, None, None, 0, None) == -5
+    # allocation-free permute: scratch need beyond its static array
+    assert lib.moe_permute_noalloc(P, 128 * 257, 2, 1024, 1, P, P, P, P, None, None) == -2
     # combine: K too large, d not a multiple of 8
     assert lib.moe_combine(P, 8, P, P, 4, 33, 128, -1, P, None, None) == -2
     assert lib.moe_combine(P, 8, P, P, 4, 4, 100, -1, P, None, None) == -1
