@@ -38,7 +38,7 @@ import workloads
 METRIC = "MoE-layer fwd tokens/s & FP8 TFLOPS at V3 shape; % of B300 FP8/HBM roofline"
 GAMMA = 0.001
 # the kernel sources the committed DRAM-traffic figure was measured with
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gate_up_v3_traffic.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fp8_gemm_gate_up_v3_traffic.txt")
 GEMM_SOURCES = ["fp8_block_scaled_bias_b300/csrc/gemm_fp8.cu",
                 "fp8_block_scaled_bias_b300/csrc/common.cuh"]
 
@@ -192,12 +192,17 @@ def committed_traffic():
     """DRAM bytes per gate/up launch from the committed ncu summary, if it was taken with
     the current kernel source; else None."""
     try:
-        t = json.load(open(TRAFFIC_FILE))
-    except Exception:
+        t = {}
+        for line in open(TRAFFIC_FILE):
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                t[k.strip()] = v.strip()
+    except OSError:
         return None
     if t.get("kernel_source_sha256_16") != gemm_source_hash():
         return None
-    return t.get("dram_bytes_per_launch_v3")
+    v = t.get("dram_bytes_per_launch_v3")
+    return int(v) if v else None
 
 
 # ---- our arm -----------------------------------------------------------------------------
