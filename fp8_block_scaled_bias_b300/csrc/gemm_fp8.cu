@@ -424,18 +424,23 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
           if (!mbar_wait_warp(tfull_bar(b), bph, abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
           const uint32_t tb = tmem_base + lane_addr + static_cast<uint32_t>(b * BN);
+          // two 16-column loads in flight per wait: four TMEM round trips per K block
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
+          for (int c = 0; c < 8; c += 2) {
             const float sc = (c < 4) ? sc0 : sc1;
             const float2 sc2 = make_float2(sc, sc);
-            uint32_t v[16];
-            tmem_ld_32x32b_x16(tb + static_cast<uint32_t>(cols[c]), v);
+            uint32_t v[2][16];
+            tmem_ld_32x32b_x16(tb + static_cast<uint32_t>(cols[c]), v[0]);
+            tmem_ld_32x32b_x16(tb + static_cast<uint32_t>(cols[c + 1]), v[1]);
             tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              acc2[c * 8 + i] = __ffma2_rn(
-                  sc2, make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])),
-                  acc2[c * 8 + i]);
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                acc2[(c + h) * 8 + i] = __ffma2_rn(
+                    sc2,
+                    make_float2(__uint_as_float(v[h][2 * i]), __uint_as_float(v[h][2 * i + 1])),
+                    acc2[(c + h) * 8 + i]);
           }
           tc_fence_before();
           __syncwarp();
