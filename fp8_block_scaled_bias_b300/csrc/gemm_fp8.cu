@@ -397,6 +397,10 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
       ++pf_it;
     };
     for (int i = 0; i < SPF - 1; ++i) prefetch_one();
+    // the scales of the first K block, read one block ahead from then on
+    cp_async_wait<SPF - 2>();
+    __syncwarp();
+    float nsa = ring_a_f[0], nsb0 = ring_b_f[0], nsb1 = ring_b_f[1];
 
     uint32_t it = 0;
     int ucount = 0;
@@ -412,17 +416,13 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 64; ++i) acc2[i] = make_float2(0.0f, 0.0f);
         for (int kb = 0; kb < KB; ++kb, ++it) {
-          prefetch_one();                                // K block it + SPF - 1
-          cp_async_wait<SPF - 1>();                      // this thread's copies for `it` landed
-          __syncwarp();                                  // lane 0's weight scales too
-          const int slot = static_cast<int>(it % SPF);
-          const float sa = ring_a_f[slot * EPI_THREADS];
-          const float sc0 = __fmul_rn(sa, ring_b_f[slot * EPI_WARPS * 2]);
-          const float sc1 = __fmul_rn(sa, ring_b_f[slot * EPI_WARPS * 2 + 1]);
+          const float sa = nsa, sb0 = nsb0, sb1 = nsb1;
           const int b = it % TBUF;
           const uint32_t bph = (it / TBUF) & 1;
           if (!mbar_wait_warp(tfull_bar(b), bph, abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
+          const float sc0 = __fmul_rn(sa, sb0);
+          const float sc1 = __fmul_rn(sa, sb1);
           const uint32_t tb = tmem_base + lane_addr + static_cast<uint32_t>(b * BN);
           // two 16-column loads in flight per wait: four TMEM round trips per K block
 #pragma unroll
@@ -445,6 +445,14 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(tempty_bar(b));     // the buffer is folded in
+          // scales of K block it + 1: their shared-memory latency overlaps the next wait
+          prefetch_one();                                // K block it + SPF - 1
+          cp_async_wait<SPF - 2>();                      // this thread's copies for it + 1
+          __syncwarp();                                  // lane 0's weight scales too
+          const int nslot = static_cast<int>((it + 1) % SPF);
+          nsa = ring_a_f[nslot * EPI_THREADS];
+          nsb0 = ring_b_f[nslot * EPI_WARPS * 2];
+          nsb1 = ring_b_f[nslot * EPI_WARPS * 2 + 1];
         }
         if (!ok) break;
         float* acc = reinterpret_cast<float*>(acc2);
