@@ -20,8 +20,9 @@ Sources, cited by page title and section:
   precision, items (a)-(d)).
 * The DeepSeek-V3 book (slop-6tp.pages.dev/papers-html/dsv3) -- ch. 2 "RMSNorm and
   SwiGLU", ch. 7 "Fine-grained and Shared Experts", ch. 8 "Routing and Load
-  Balancing", ch. 15 "Moving Tokens to Experts", ch. 16 "Understanding FP8
-  Numbers", ch. 17 "The Actual Mixed-precision Pipeline".
+  Balancing" (including "The complementary sequence loss"), ch. 15 "Moving Tokens to
+  Experts", ch. 16 "Understanding FP8 Numbers", ch. 17 "The Actual Mixed-precision
+  Pipeline".
 
 Modules:
   formats  -- E4M3 (fn variant) codec and BF16 rounding
@@ -30,6 +31,7 @@ Modules:
   permute  -- stable grouping of (token, slot) pairs into expert segments
   gemm     -- block-scaled GEMM with per-128-K promotion, SwiGLU expert, combine
   layer    -- the whole layer forward, and a per-token variant for large shapes
+  balance  -- sequence-wise balance statistics f_i, P_i and the complementary loss
 
 Parity pins live in ``tests/test_oracle_*.py``.  Functions without an independent
 pin say "parity unpinned" in their docstring.
@@ -42,11 +44,12 @@ from .router import router_logits, sigmoid_f32, route, route_token, bias_update
 from .permute import permute
 from .gemm import blockscaled_gemm, swiglu_expert, combine
 from .layer import moe_layer, moe_layer_tokens
+from .balance import plain_topk, seq_balance_stats
 
 __all__ = [
     "E4M3_MAX", "E4M3_MIN_NORMAL", "e4m3_decode", "e4m3_decode_table", "e4m3_encode",
     "e4m3_round", "bf16_round", "quant_1x128", "quant_128x128", "dequant_1x128",
     "dequant_128x128", "router_logits", "sigmoid_f32", "route", "route_token",
     "bias_update", "permute", "blockscaled_gemm", "swiglu_expert", "combine",
-    "moe_layer", "moe_layer_tokens",
+    "moe_layer", "moe_layer_tokens", "plain_topk", "seq_balance_stats",
 ]

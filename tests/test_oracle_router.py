@@ -70,6 +70,23 @@ def test_route_matches_brute_force():
             assert {e // (E // G) for e in idx[t]} <= groups
 
 
+def test_group_score_over_every_expert_of_the_group():
+    # the variant that scores a group by the sum of all its members' scores is the
+    # group_topn = E / n_groups case; pinned against exhaustive search
+    rng = np.random.default_rng(2)
+    for (E, G, M, K) in [(16, 4, 2, 4), (12, 3, 2, 3), (16, 8, 3, 5)]:
+        z = rng.standard_normal((40, E)).astype(np.float32) * 2
+        b = (rng.uniform(-0.3, 0.3, E)).astype(np.float32)
+        idx, _ = oracle.route(z, b, G, M, E // G, K)
+        c = (oracle.sigmoid_f32(z) + b).astype(np.float32)
+        for t in range(40):
+            chosen, groups = _brute_force(c[t], G, M, E // G, K)
+            assert set(idx[t]) == chosen
+            gs = E // G
+            sums = [float(c[t, g * gs:(g + 1) * gs].astype(np.float64).sum()) for g in range(G)]
+            assert groups == set(sorted(range(G), key=lambda g: (-sums[g], g))[:M])
+
+
 def test_no_group_limit_reduces_to_textbook_topk():
     rng = np.random.default_rng(1)
     s = rng.uniform(0, 1, (64, 32)).astype(np.float32)
