@@ -28,6 +28,7 @@ SIGNATURES = {
     "moe_permute_ws_bytes": (_SZ, [_I, _I, _I]),
     "moe_permute_noalloc": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
     "fp8_quant_1x128": (_I, [_P, _I, _I, _I, _P, _P, _P]),
+    "fp8_quant_scatter_1x128": (_I, [_P, _I, _I, _I, _P, _I, _I, _I, _P, _P, _P, _P]),
     "fp8_quant_128x128": (_I, [_P, _I, _I, _P, _P, _P]),
     "fp8_blockscaled_grouped_gemm": (_I, [_P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P, _I,
                                           _P, _P, _SZ, _P]),
@@ -39,6 +40,8 @@ SIGNATURES = {
     "moe_gate_up_fp8": (_I, [_P, _P, _P, _I, _P, _P, _I, _I, _I, _P, _P, _P, _P]),
     "moe_combine": (_I, [_P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _P]),
     "moe_bias_update": (_I, [_P, _P, _I, _I, _I, _F, _P]),
+    "moe_seq_balance_stats": (_I, [_P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _SZ, _P]),
+    "moe_seq_balance_stats_ws_bytes": (_SZ, [_I, _I, _I]),
     "moe_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
 }
 

@@ -129,6 +129,19 @@ int fp8_quant_1x128(const uint16_t* x, int rows, int cols, int ldx, uint8_t* q, 
   return moe::launch_quant_1x128(x, rows, cols, ldx, q, scale, as_stream(stream));
 }
 
+int fp8_quant_scatter_1x128(const uint16_t* x, int T, int cols, int ldx, const int32_t* row_of,
+                            int K, int shared_row_base, int n_rows, uint8_t* q, float* scale,
+                            int32_t* dev_status, void* stream) {
+  if (T < 0 || K < 0 || n_rows < 0 || cols < 0 || cols % 128 != 0 || ldx < cols || ldx % 8 != 0)
+    return MOE_ERR_INVALID_ARG;
+  if (T == 0 || cols == 0) return MOE_OK;
+  if (!x || (K > 0 && !row_of) || !q || !scale || !aligned16(x) ||
+      (reinterpret_cast<uintptr_t>(q) & 7u))
+    return MOE_ERR_INVALID_ARG;
+  return moe::launch_quant_scatter_1x128(x, T, cols, ldx, row_of, K, shared_row_base, n_rows, q,
+                                         scale, dev_status, as_stream(stream));
+}
+
 int fp8_quant_128x128(const float* w, int rows, int cols, uint8_t* q, float* scale,
                       void* stream) {
   if (rows < 0 || cols < 0 || rows % 128 != 0 || cols % 128 != 0) return MOE_ERR_INVALID_ARG;
@@ -281,6 +294,25 @@ int moe_bias_update(float* bias, const int32_t* counts, int E, int T, int K, flo
   if (E < 1 || T < 0 || K < 1) return MOE_ERR_INVALID_ARG;
   if (!bias || !counts) return MOE_ERR_INVALID_ARG;
   return moe::launch_bias_update(bias, counts, E, T, K, gamma, as_stream(stream));
+}
+
+size_t moe_seq_balance_stats_ws_bytes(int T, int E, int seq_len) {
+  if (T <= 0 || E <= 0 || seq_len <= 0 || T % seq_len != 0) return 0;
+  return moe::seq_balance_ws_bytes(T, E, seq_len);
+}
+
+int moe_seq_balance_stats(const float* scores, int scores_are_affinities, int T, int E, int K,
+                          int seq_len, float alpha, float* f, float* P, float* loss, void* ws,
+                          size_t ws_bytes, void* stream) {
+  if (T < 0 || E < 1 || K < 1 || K > E || seq_len < 1 || T % seq_len != 0)
+    return MOE_ERR_INVALID_ARG;
+  if (E > 1024 || K > 32 || T / seq_len > 65535) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!scores || !f || !P || !loss) return MOE_ERR_INVALID_ARG;
+  const size_t need = moe::seq_balance_ws_bytes(T, E, seq_len);
+  if (!ws || ws_bytes < need) return MOE_ERR_WORKSPACE;
+  return moe::launch_seq_balance(scores, scores_are_affinities, T, E, K, seq_len, alpha, f, P,
+                                 loss, ws, as_stream(stream));
 }
 
 size_t moe_workspace_bytes(int T, int K, int E, int d, int f) {

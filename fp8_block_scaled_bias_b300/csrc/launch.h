@@ -17,6 +17,11 @@ int check_launch();
 
 int launch_quant_1x128(const uint16_t* x, int rows, int cols, int ldx, uint8_t* q,
                        float* scale, cudaStream_t stream);
+// Quantise each row t of x (BF16 [T][cols], row stride ldx) once and write it to rows
+// row_of[t][0..K-1] and, if shared_row_base >= 0, shared_row_base + t of q / scale.
+int launch_quant_scatter_1x128(const uint16_t* x, int T, int cols, int ldx, const int32_t* row_of,
+                               int K, int shared_row_base, int n_rows, uint8_t* q, float* scale,
+                               int32_t* status, cudaStream_t stream);
 int launch_quant_128x128(const float* w, int rows, int cols, uint8_t* q, float* scale,
                          cudaStream_t stream);
 
@@ -37,6 +42,11 @@ int permute_noalloc_scratch(int32_t** out);
 int launch_combine(const uint16_t* y_rows, int n_rows, const int32_t* row_of,
                    const float* gate, int T, int K, int d, int shared_row_base, uint16_t* y,
                    int32_t* status, cudaStream_t stream);
+
+// Sequence-wise balance statistics (balance.cu): workspace bytes and the two launches.
+size_t seq_balance_ws_bytes(int T, int E, int L);
+int launch_seq_balance(const float* scores, int aff, int T, int E, int K, int L, float alpha,
+                       float* f, float* P, float* loss, void* ws, cudaStream_t stream);
 
 int launch_bias_update(float* bias, const int32_t* counts, int E, int T, int K, float gamma,
                        cudaStream_t stream);

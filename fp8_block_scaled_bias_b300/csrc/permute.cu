@@ -6,7 +6,7 @@
 // A stable counting sort keyed by expert, in three passes over token chunks:
 //   count    per-chunk histograms
 //   scan     per-expert totals, exclusive scan -> segment offsets, per-chunk bases
-//   scatter  thread e walks the chunk's pairs in (token, slot) order and hands out rows
+//   scatter  warps walk the chunk's pairs in (token, slot) order and hand out rows
 // Every step is integer work in a fixed order, so the result is deterministic and equal
 // to a stable sort whatever the launch timing.
 #include <mutex>
@@ -19,6 +19,7 @@ namespace moe {
 namespace {
 constexpr int kChunkTokens = 128;
 constexpr int kPermThreads = 256;
+constexpr int kPermWarps = kPermThreads / 32;
 constexpr int kScanThreads = 1024;
 
 int n_chunks(int T) { return (T + kChunkTokens - 1) / kChunkTokens; }
@@ -100,28 +101,57 @@ __global__ void __launch_bounds__(kScanThreads) permute_scan_kernel(
   }
 }
 
+// One block per chunk.  The chunk's pairs are split into kPermWarps contiguous runs, one
+// per warp; a per-warp histogram and a prefix over the warps give each warp its first row
+// in every expert segment.  Each warp then walks its run in windows of 32 pairs, in
+// order: lanes holding the same expert find each other with __match_any_sync, take rows
+// in lane order, and the highest such lane advances that expert's running row.  The rows
+// handed out are those of a stable counting sort, independent of timing.
 __global__ void __launch_bounds__(kPermThreads) permute_scatter_kernel(
     const int32_t* __restrict__ idx, int T, int K, int E, int include_shared,
     const int32_t* __restrict__ chunk_base, int32_t* __restrict__ row_token,
     int32_t* __restrict__ row_of) {
-  extern __shared__ int32_t pairs[];
+  extern __shared__ int32_t next_row[];        // [kPermWarps][E]
   const int c = blockIdx.x;
   const int t0 = c * kChunkTokens;
   const int nt = min(kChunkTokens, T - t0);
   const int np = nt * K;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int run = ((np + kPermWarps - 1) / kPermWarps + 31) & ~31;
+  const int p_begin = min(np, warp * run), p_end = min(np, p_begin + run);
   const int32_t* src = idx + static_cast<long long>(t0) * K;
-  for (int p = threadIdx.x; p < np; p += blockDim.x) pairs[p] = src[p];
+  for (int i = threadIdx.x; i < kPermWarps * E; i += blockDim.x) next_row[i] = 0;
+  __syncthreads();
+  for (int p = p_begin + lane; p < p_end; p += 32) {
+    const int e = src[p];
+    if (e >= 0 && e < E) atomicAdd(&next_row[warp * E + e], 1);   // counts: order-free
+  }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int row = chunk_base[static_cast<long long>(c) * E + e];
-    for (int p = 0; p < np; ++p) {             // (token, slot) order: stable
-      if (pairs[p] == e) {
-        const int t = t0 + p / K;
-        row_of[static_cast<long long>(t0) * K + p] = row;
-        row_token[row] = t;
-        ++row;
-      }
+    for (int w = 0; w < kPermWarps; ++w) {
+      const int n = next_row[w * E + e];
+      next_row[w * E + e] = row;
+      row += n;
     }
+  }
+  __syncthreads();
+  int32_t* mine = next_row + warp * E;
+  const unsigned lt = (1u << lane) - 1u;
+  for (int base = p_begin; base < p_end; base += 32) {
+    const int p = base + lane;
+    int e = p < p_end ? src[p] : -1;
+    const bool valid = e >= 0 && e < E;
+    if (!valid) e = -1 - lane;                 // a key no other lane holds
+    const unsigned same = __match_any_sync(0xFFFFFFFFu, e);
+    if (valid) {
+      const int row = mine[e] + __popc(same & lt);
+      row_of[static_cast<long long>(t0) * K + p] = row;
+      row_token[row] = t0 + p / K;
+    }
+    __syncwarp();
+    if (valid && lane == 31 - __clz(same)) mine[e] += __popc(same);
+    __syncwarp();
   }
   if (include_shared) {
     const long long base = static_cast<long long>(T) * K;
@@ -143,7 +173,7 @@ int launch_permute(const int32_t* idx, int T, int K, int E, int include_shared,
                                                        offsets);
   if (check_launch() != MOE_OK) return MOE_ERR_CUDA;
   if (nc > 0) {
-    const size_t smem = static_cast<size_t>(kChunkTokens) * K * sizeof(int32_t);
+    const size_t smem = static_cast<size_t>(kPermWarps) * E * sizeof(int32_t);
     permute_scatter_kernel<<<nc, kPermThreads, smem, stream>>>(idx, T, K, E, include_shared,
                                                                 chunk, row_token, row_of);
     if (check_launch() != MOE_OK) return MOE_ERR_CUDA;

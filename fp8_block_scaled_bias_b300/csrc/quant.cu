@@ -59,6 +59,75 @@ __global__ void __launch_bounds__(256) quant_1x128_kernel(const uint16_t* __rest
   }
 }
 
+// Quantise-and-dispatch: each token's row of x is quantised 1x128 once and written to
+// every row that uses it -- its K routed rows row_of[t][k] and, when shared_row_base >=
+// 0, its shared-expert row shared_row_base + t -- of the permuted activation matrix (the
+// pages quantise activations before dispatch, "DeepSeek-V3" book, ch. 17 "FP8 dispatch,
+// BF16 combine").  Bit for bit the same as quant_1x128_kernel followed by a row gather
+// with the inverse map: the same per-tile arithmetic, written to more places.
+// One block per token (grid-stride); a half-warp per 1x128 tile.
+__global__ void __launch_bounds__(256) quant_scatter_1x128_kernel(
+    const uint16_t* __restrict__ x, int T, int ldx, int ncb, const int32_t* __restrict__ row_of,
+    int K, int shared_row_base, int n_rows, uint8_t* __restrict__ q, float* __restrict__ scale,
+    int32_t* status) {
+  const int hw = threadIdx.x >> 4;            // half-warp: 16 per block
+  const int hl = threadIdx.x & 15;
+  const long long cols = static_cast<long long>(ncb) * 128;
+  const int ndst = K + (shared_row_base >= 0 ? 1 : 0);
+  for (int t = blockIdx.x; t < T; t += gridDim.x) {
+    for (int cb0 = 0; cb0 < ncb; cb0 += 16) {  // uniform trip count: shuffles stay full-warp
+      const int cb = cb0 + hw;
+      const bool valid = cb < ncb;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (valid)
+        v = __ldcs(reinterpret_cast<const uint4*>(x + static_cast<long long>(t) * ldx + cb * 128 +
+                                                  hl * 8));
+      float f[8];
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+      }
+      float amax = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+#pragma unroll
+      for (int off = 8; off > 0; off >>= 1)
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+      const float s = e4m3_scale_from_amax(amax);
+      uint32_t out[2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const uint32_t a = f32x2_to_e4m3x2(__fdiv_rn(f[4 * i], s), __fdiv_rn(f[4 * i + 1], s));
+        const uint32_t b = f32x2_to_e4m3x2(__fdiv_rn(f[4 * i + 2], s), __fdiv_rn(f[4 * i + 3], s));
+        out[i] = a | (b << 16);
+      }
+      if (!valid) continue;
+      for (int k = 0; k < ndst; ++k) {
+        const int r = k < K ? row_of[static_cast<long long>(t) * K + k] : shared_row_base + t;
+        if (r < 0 || r >= n_rows) {
+          if (hl == 0 && cb == 0) set_status(status, MOE_ERR_DEVICE_DATA);
+          continue;
+        }
+        *reinterpret_cast<uint2*>(q + r * cols + cb * 128 + hl * 8) = make_uint2(out[0], out[1]);
+        if (hl == 0) scale[static_cast<long long>(cb) * n_rows + r] = s;
+      }
+    }
+  }
+}
+
+int launch_quant_scatter_1x128(const uint16_t* x, int T, int cols, int ldx, const int32_t* row_of,
+                               int K, int shared_row_base, int n_rows, uint8_t* q, float* scale,
+                               int32_t* status, cudaStream_t stream) {
+  if (T == 0 || cols == 0) return MOE_OK;
+  const int cap = num_sms() * 8;
+  const int blocks = T < cap ? T : cap;
+  quant_scatter_1x128_kernel<<<blocks, 256, 0, stream>>>(x, T, ldx, cols / 128, row_of, K,
+                                                         shared_row_base, n_rows, q, scale, status);
+  return check_launch();
+}
+
 // One block per 128x128 weight block; thread t covers row t/2, 64 columns.
 __global__ void __launch_bounds__(256) quant_128x128_kernel(const float* __restrict__ w,
                                                              int rows, int cols,

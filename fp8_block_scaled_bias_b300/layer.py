@@ -94,8 +94,6 @@ class MoELayer:
         self.offsets = emp(E + 2, dt=torch.int32)
         self.row_token = emp(self.rows, dt=torch.int32)
         self.row_of = emp(T, K, dt=torch.int32)
-        self.xq = emp(T, d, dt=torch.uint8)
-        self.sx = emp(d // 128, T)
         self.xq_rows = emp(self.rows, d, dt=torch.uint8)
         self.sx_rows = emp(d // 128, self.rows)
         self.hq = emp(self.rows, f, dt=torch.uint8)
@@ -106,7 +104,7 @@ class MoELayer:
         self.seg_end = self.offsets[cfg.E + 1:cfg.E + 2]     # device int32: rows in use
 
     # kernel launches of one forward, by stage (bias_update adds one more)
-    STAGE_LAUNCHES = {"router_logits": 1, "route": 1, "permute": 3, "quant": 1, "gather": 1,
+    STAGE_LAUNCHES = {"router_logits": 1, "route": 1, "permute": 3, "quant_dispatch": 1,
                       "gate_up": 1, "down": 1, "combine": 1}
 
     def forward(self, x, logits=None, residual=False, mark=None):
@@ -127,11 +125,10 @@ class MoELayer:
         ops.permute(self.idx, cfg.E, True, self.status,
                     out=(self.counts, self.offsets, self.row_token, self.row_of))
         mark("permute")
-        ops.quant_1x128(x, out=(self.xq, self.sx))
-        mark("quant")
-        ops.gather_rows(self.xq, self.sx, self.row_token, self.seg_end, self.status,
-                        out=(self.xq_rows, self.sx_rows))
-        mark("gather")
+        # 1x128 quantisation straight into segment order (one pass over x)
+        ops.quant_scatter_1x128(x, self.row_of, self.rows, self.T * cfg.K, self.status,
+                                out=(self.xq_rows, self.sx_rows))
+        mark("quant_dispatch")
         ops.gate_up(self.xq_rows, self.sx_rows, self.offsets, w.w13, w.s13, self.status,
                     out=(self.hq, self.sh))
         mark("gate_up")

@@ -114,6 +114,26 @@ def bias_update(bias, counts, T, K, gamma):
     return bias
 
 
+def seq_balance_stats(scores, K, seq_len, alpha=1e-4, affinities=False, out=None):
+    """(f [S, E], P [S, E], loss [S]) FP32 statistics of the sequence-wise balance loss for
+    scores [T, E] (logits, or affinities), S = T / seq_len sequences."""
+    _check(scores, _F32, "scores", 2)
+    T, E = scores.shape
+    S = T // seq_len if seq_len > 0 else 0
+    dev = scores.device
+    if out is None:
+        f = torch.empty(S, E, dtype=_F32, device=dev)
+        P = torch.empty(S, E, dtype=_F32, device=dev)
+        loss = torch.empty(S, dtype=_F32, device=dev)
+    else:
+        f, P, loss = out
+    lib = load()
+    ws, wsb = WS.get(lib.moe_seq_balance_stats_ws_bytes(T, E, seq_len), dev)
+    call("moe_seq_balance_stats", _ptr(scores), int(bool(affinities)), T, E, K, seq_len,
+         float(alpha), _ptr(f), _ptr(P), _ptr(loss), ws, wsb, _stream())
+    return f, P, loss
+
+
 # ---- dispatch ---------------------------------------------------------------------------
 
 def permute(idx, E, include_shared=True, status=None, out=None):
@@ -148,6 +168,25 @@ def quant_1x128(x, out=None):
     else:
         q, s = out
     call("fp8_quant_1x128", _ptr(x), rows, cols, cols, _ptr(q), _ptr(s), _stream())
+    return q, s
+
+
+def quant_scatter_1x128(x, row_of, n_rows, shared_row_base=None, status=None, out=None):
+    """Quantise each token row of x once and write it to rows row_of[t, :] and (if
+    shared_row_base is not None) shared_row_base + t: bit for bit quant_1x128 followed by
+    gather_rows with the inverse map."""
+    _check(x, _BF16, "x", 2)
+    _check(row_of, _I32, "row_of", 2)
+    T, cols = x.shape
+    K = row_of.shape[1]
+    if out is None:
+        q = torch.empty(n_rows, cols, dtype=_U8, device=x.device)
+        s = torch.empty(cols // 128, n_rows, dtype=_F32, device=x.device)
+    else:
+        q, s = out
+    base = -1 if shared_row_base is None else int(shared_row_base)
+    call("fp8_quant_scatter_1x128", _ptr(x), T, cols, cols, _ptr(row_of), K, base, n_rows,
+         _ptr(q), _ptr(s), _ptr(status), _stream())
     return q, s
 
 

@@ -10,7 +10,8 @@
  *   moe_swiglu_fp8_fwd    grouped gate/up GEMM + SwiGLU + requantise, grouped down GEMM
  *   moe_combine           y_t = shared_t + sum_k g_tk * expert_out
  *   moe_bias_update       aux-loss-free bias step after the forward
- * plus fp8_blockscaled_grouped_gemm (the GEMM on its own, dense when G = 1) and two
+ * plus moe_seq_balance_stats (statistics of the complementary sequence-wise balance
+ * loss), fp8_blockscaled_grouped_gemm (the GEMM on its own, dense when G = 1) and two
  * setup helpers that prepare weights (fp8_quant_128x128, moe_router_split_bf16).
  *
  * Conventions shared by every entry point
@@ -157,6 +158,19 @@ int moe_permute_noalloc(const int32_t* topk_idx, int T, int K, int E, int includ
 int fp8_quant_1x128(const uint16_t* x, int rows, int cols, int ldx, uint8_t* q,
                     float* scale, void* stream);
 
+/* Quantise-and-dispatch: each token row t of x is quantised as above once and written
+ * to every row of the permuted matrix that uses it: rows row_of[t][0..K-1] and, when
+ * shared_row_base >= 0, row shared_row_base + t.  With row_of and the shared rows from
+ * moe_permute this is bit for bit fp8_quant_1x128 followed by moe_gather_rows_fp8 with
+ * row_token, in one pass over x: the pages quantise activations before dispatch ([book]
+ * ch. 17 "FP8 dispatch, BF16 combine").  x: BF16 [T][cols] (pitch ldx); row_of: int32
+ * [T][K]; q: uint8 [n_rows][cols]; scale: FP32 [cols/128][n_rows].  A destination
+ * outside [0, n_rows) sets MOE_ERR_DEVICE_DATA and is skipped.  Alignment as for
+ * fp8_quant_1x128. */
+int fp8_quant_scatter_1x128(const uint16_t* x, int T, int cols, int ldx, const int32_t* row_of,
+                            int K, int shared_row_base, int n_rows, uint8_t* q, float* scale,
+                            int32_t* dev_status, void* stream);
+
 /* Setup helper: quantise FP32 w [rows][cols] in 128x128 blocks, same scale rule.
  * q: uint8 [rows][cols]; scale: FP32 [rows/128][cols/128].  rows, cols % 128 == 0. */
 int fp8_quant_128x128(const float* w, int rows, int cols, uint8_t* q, float* scale,
@@ -251,6 +265,26 @@ int moe_combine(const uint16_t* y_rows, int n_rows, const int32_t* row_of,
  * with the comparison done exactly in integers (T*K - E*counts[i]). */
 int moe_bias_update(float* bias, const int32_t* counts, int E, int T, int K, float gamma,
                     void* stream);
+
+/* ---- sequence-wise balance statistics (forward only) ------------------------------- */
+
+/* Statistics of the complementary sequence-wise balance loss ([book] ch. 8 "The
+ * complementary sequence loss"; [sum] core idea 2, the safety-net paragraph), for
+ * T / seq_len consecutive sequences of seq_len tokens each:
+ *   s[t][i]  = scores[t][i] if scores_are_affinities, else fl32(1 / (1 + expf(-z)))
+ *   f[q][i]  = fl32(E * n_i) / fl32(K * seq_len), n_i = tokens of sequence q whose K
+ *              largest s (over all E experts, ties to the lower index; no bias, no
+ *              group limit) include expert i
+ *   P[q][i]  = (1/seq_len) * sum over the sequence of s[t][i] / sum_j s[t][j]
+ *   loss[q]  = alpha * sum_i f[q][i] * P[q][i]                 (alpha = 1e-4 in V3)
+ * All FP32, summed in a fixed order (deterministic).  scores: FP32 [T][E]; f, P: FP32
+ * [T/seq_len][E]; loss: FP32 [T/seq_len].  Workspace: moe_seq_balance_stats_ws_bytes.
+ * Errors: MOE_ERR_INVALID_ARG unless 1 <= K <= E and seq_len divides T;
+ * MOE_ERR_UNSUPPORTED for E > 1024, K > 32 or more than 65,535 sequences. */
+size_t moe_seq_balance_stats_ws_bytes(int T, int E, int seq_len);
+int moe_seq_balance_stats(const float* scores, int scores_are_affinities, int T, int E, int K,
+                          int seq_len, float alpha, float* f, float* P, float* loss, void* ws,
+                          size_t ws_bytes, void* stream);
 
 /* Workspace large enough for every call of one layer forward with these sizes. */
 size_t moe_workspace_bytes(int T, int K, int E, int d, int f);

@@ -64,6 +64,55 @@ def test_quant_1x128_strided_input():
     assert np.array_equal(q.cpu().numpy(), q_ref) and np.array_equal(s.cpu().numpy(), s_ref)
 
 
+@pytest.mark.parametrize("T,K,cols,shared", [(5, 3, 384, True), (300, 8, 512, True),
+                                              (257, 1, 128, False), (1, 4, 7168, True)])
+def test_quant_scatter_bit_exact(T, K, cols, shared):
+    """Every row a token is dispatched to holds the oracle's 1x128 quantisation of that
+    token; rows nobody is dispatched to are left untouched."""
+    x = _wide_range_bf16(T, cols, seed=T + K)
+    rng = np.random.default_rng(T)
+    n_rows = T * K + (T if shared else 0) + 3                   # 3 rows nobody writes
+    row_of = rng.permutation(T * K).astype(np.int32).reshape(T, K)
+    q = torch.full((n_rows, cols), 0xAB, dtype=torch.uint8, device=DEV)
+    sc = torch.full((cols // 128, n_rows), -1.0, dtype=torch.float32, device=DEV)
+    status = ops.new_status(DEV)
+    ops.quant_scatter_1x128(x.to(DEV), torch.from_numpy(row_of).to(DEV), n_rows,
+                            T * K if shared else None, status, out=(q, sc))
+    assert ops.status_value(status) == 0
+    q_ref, s_ref = oracle.quant_1x128(x.float().numpy())
+    qg, sg = q.cpu().numpy(), sc.cpu().numpy()
+    for t in range(T):
+        for r in list(row_of[t]) + ([T * K + t] if shared else []):
+            assert np.array_equal(qg[r], q_ref[t]) and np.array_equal(sg[:, r], s_ref[:, t])
+    used = T * K + (T if shared else 0)
+    assert (qg[used:] == 0xAB).all() and (sg[:, used:] == -1.0).all()
+
+
+def test_quant_scatter_v3_matches_quant_then_gather():
+    cfg = workloads.V3
+    x = workloads.gen_x(cfg).to(DEV)
+    g = torch.Generator().manual_seed(4)
+    idx = torch.stack([torch.randperm(cfg.E, generator=g)[:cfg.K] for _ in range(cfg.T)])
+    counts, offsets, row_token, row_of = ops.permute(idx.int().to(DEV), cfg.E, True)
+    q, s = ops.quant_1x128(x)
+    want = ops.gather_rows(q, s, row_token)
+    got = ops.quant_scatter_1x128(x, row_of, cfg.rows, cfg.T * cfg.K)
+    assert torch.equal(got[0], want[0]) and torch.equal(got[1], want[1])
+
+
+def test_quant_scatter_bad_row_sets_status():
+    x = _wide_range_bf16(2, 256, seed=1).to(DEV)
+    row_of = torch.tensor([[0, 9], [3, -1]], dtype=torch.int32, device=DEV)
+    q = torch.zeros(4, 256, dtype=torch.uint8, device=DEV)
+    sc = torch.zeros(2, 4, dtype=torch.float32, device=DEV)
+    status = ops.new_status(DEV)
+    ops.quant_scatter_1x128(x, row_of, 4, None, status, out=(q, sc))
+    assert ops.status_value(status) == -6
+    q_ref, s_ref = oracle.quant_1x128(x.float().cpu().numpy())
+    assert np.array_equal(q.cpu().numpy()[[0, 3]], q_ref)
+    assert (q.cpu().numpy()[[1, 2]] == 0).all() and (sc.cpu().numpy()[:, [1, 2]] == 0).all()
+
+
 @pytest.mark.parametrize("rows,cols", [(128, 128), (256, 512), (2048, 7168)])
 def test_quant_128x128_bit_exact(rows, cols):
     g = torch.Generator().manual_seed(rows + cols)
@@ -126,6 +175,22 @@ def test_route_other_shapes_and_route_scale():
                                         scores_are_affinities=True)
             assert np.array_equal(idx.cpu().numpy(), i_ref), (E, G, M, K)
             assert np.array_equal(gate.cpu().numpy(), g_ref), (E, G, M, K)
+
+
+@pytest.mark.parametrize("cfg", [workloads.TINY, workloads.V3], ids=["tiny", "v3"])
+@pytest.mark.parametrize("group_topn", ["all", 1])
+def test_route_group_score_variants(cfg, group_topn):
+    """Group scored by the sum over all its members (group_topn = E / n_groups) or by its
+    best member alone, bit-exact against the oracle."""
+    n = cfg.E // cfg.n_groups if group_topn == "all" else group_topn
+    s = _affinities_with_ties(1024, cfg.E, 11)
+    b = workloads.gen_bias(cfg).numpy()
+    idx, gate = ops.route(torch.from_numpy(s).to(DEV), torch.from_numpy(b).to(DEV),
+                          cfg.n_groups, cfg.topk_groups, cfg.K, group_topn=n, affinities=True)
+    i_ref, g_ref = oracle.route(s, b, cfg.n_groups, cfg.topk_groups, n, cfg.K,
+                                scores_are_affinities=True)
+    assert np.array_equal(idx.cpu().numpy(), i_ref)
+    assert np.array_equal(gate.cpu().numpy(), g_ref)
 
 
 @pytest.mark.parametrize("cfg", [workloads.TINY, workloads.V3], ids=["tiny", "v3"])

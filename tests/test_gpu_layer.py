@@ -53,9 +53,13 @@ def _compare_tiny(cfg, layer, ref, x, gate_tol=None):
     """gate_tol None: identical logits on both sides, gates within 16 float32 ulps;
     else an absolute tolerance (the GPU routed from its own logits)."""
     T, K = cfg.T, cfg.K
-    for name in ("idx", "counts", "offsets", "row_token", "row_of", "xq", "sx"):
+    for name in ("idx", "counts", "offsets", "row_token", "row_of"):
         got = getattr(layer, name).cpu().numpy()
         assert np.array_equal(got, ref[name]), name
+    # the quantised activations, already in segment order
+    tok = ref["row_token"]
+    assert np.array_equal(layer.xq_rows.cpu().numpy(), ref["xq"][tok])
+    assert np.array_equal(layer.sx_rows.cpu().numpy(), ref["sx"][:, tok])
     # from logits the GPU sigmoid uses expf: gates agree to a few float32 ulps
     g = layer.gate.cpu().numpy()
     if gate_tol is None:
@@ -81,8 +85,13 @@ def test_tiny_layer_from_identical_logits(tiny):
     ref = oracle.moe_layer(x.float().numpy(), w.centroids.cpu().numpy(), w.bias.cpu().numpy(),
                            ex, cfg.n_groups, cfg.topk_groups, cfg.K, logits=logits.numpy())
     _compare_tiny(cfg, layer, ref, x)
+    # quantise-in-gather (the layer's path) equals quantise, then gather: identical bits
+    xq, sx = ops.quant_1x128(x.to(DEV))
+    xq_rows, sx_rows = ops.gather_rows(xq, sx, layer.row_token, layer.seg_end, layer.status)
+    torch.cuda.synchronize()
+    assert torch.equal(xq_rows, layer.xq_rows) and torch.equal(sx_rows, layer.sx_rows)
     # the one-call expert entry point runs the same kernels: identical bits
-    hq, sh, y_rows = ops.swiglu_fwd(layer.xq, layer.sx, layer.row_token, layer.offsets,
+    hq, sh, y_rows = ops.swiglu_fwd(xq, sx, layer.row_token, layer.offsets,
                                     layer.rows, w.w13, w.s13, w.w2, w.s2, layer.status)
     torch.cuda.synchronize()
     assert torch.equal(hq, layer.hq) and torch.equal(sh, layer.sh)
