@@ -39,7 +39,8 @@ pin say "parity unpinned" in their docstring.
 
 from .formats import (E4M3_MAX, E4M3_MIN_NORMAL, e4m3_decode, e4m3_decode_table,
                       e4m3_encode, e4m3_round, bf16_round)
-from .quant import quant_1x128, quant_128x128, dequant_1x128, dequant_128x128
+from .quant import (quant_1x128, quant_128x128, dequant_1x128, dequant_128x128,
+                    quant_1x128_pow2, quant_128x128_pow2)
 from .router import router_logits, sigmoid_f32, route, route_token, bias_update
 from .permute import permute
 from .gemm import blockscaled_gemm, swiglu_expert, combine
@@ -49,7 +50,7 @@ from .balance import plain_topk, seq_balance_stats
 __all__ = [
     "E4M3_MAX", "E4M3_MIN_NORMAL", "e4m3_decode", "e4m3_decode_table", "e4m3_encode",
     "e4m3_round", "bf16_round", "quant_1x128", "quant_128x128", "dequant_1x128",
-    "dequant_128x128", "router_logits", "sigmoid_f32", "route", "route_token",
+    "dequant_128x128", "quant_1x128_pow2", "quant_128x128_pow2", "router_logits", "sigmoid_f32", "route", "route_token",
     "bias_update", "permute", "blockscaled_gemm", "swiglu_expert", "combine",
     "moe_layer", "moe_layer_tokens", "plain_topk", "seq_balance_stats",
 ]

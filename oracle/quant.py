@@ -21,6 +21,15 @@ Saturation is required: x/s for the max element can round to just above 448.
 
 Layouts: activation scales are stored K-block-major, ``s[col_block][row]``; weight
 scales ``s[row_block][col_block]``.
+
+Power-of-two variant (the MX-native path).  The pages note that the 1x128 / 128x128
+groups match the microscaling formats Blackwell tensor cores take natively ("DeepSeek-V3"
+summary, core idea 6(a)), list native group-scaled MMA on the hardware wishlist (core
+idea 8), and mention power-of-two scales as a way to avoid extra quantisation error
+(DeepSeek-V3 book, ch. 17 "Attention-related saved activations").  Reading taken:
+  s = the smallest power of two with 448 * s >= amax   (s = 1 when amax == 0)
+  q = E4M3_rne(x / s)        (the division is exact; |x / s| <= 448, so no saturation)
+with the same group shapes and layouts; the tensor core reads the scale's exponent byte.
 """
 
 import numpy as np
@@ -32,6 +41,45 @@ def _scale_from_amax(amax):
     amax = np.asarray(amax, dtype=np.float32)
     s = amax / np.float32(E4M3_MAX)                 # float32 / float32 -> float32, RNE
     return np.where(amax == 0, np.float32(1.0), s).astype(np.float32)
+
+
+def _pow2_scale_from_amax(amax):
+    """Smallest power of two s with 448 * s >= amax (exact comparisons); 1 for amax == 0."""
+    amax = np.asarray(amax, dtype=np.float64)
+    out = np.ones(amax.shape, dtype=np.float64)
+    for i, a in np.ndenumerate(amax):
+        if a == 0:
+            continue
+        e = int(np.ceil(np.log2(a / E4M3_MAX)))
+        while E4M3_MAX * 2.0 ** (e - 1) >= a:         # step down while still large enough
+            e -= 1
+        while E4M3_MAX * 2.0 ** e < a:                # step up until large enough
+            e += 1
+        out[i] = 2.0 ** e
+    return out.astype(np.float32)
+
+
+def _quant_groups(x, group_shape, scale_fn):
+    """Shared shape handling: x [rows, cols] in (gr, gc) groups -> (q, s[rows/gr, cols/gc])."""
+    x = np.asarray(x, dtype=np.float32)
+    rows, cols = x.shape
+    gr, gc = group_shape
+    xb = x.reshape(rows // gr, gr, cols // gc, gc)
+    amax = np.abs(xb).max(axis=(1, 3))
+    s = scale_fn(amax)
+    v = (xb / s[:, None, :, None]).astype(np.float32)
+    return e4m3_encode(v).reshape(rows, cols), s
+
+
+def quant_1x128_pow2(x):
+    """Power-of-two-scale variant of quant_1x128: (q uint8[rows, cols], s[cols/128, rows])."""
+    q, s = _quant_groups(x, (1, 128), _pow2_scale_from_amax)
+    return q, np.ascontiguousarray(s.T)
+
+
+def quant_128x128_pow2(w):
+    """Power-of-two-scale variant of quant_128x128: (q, s[rows/128, cols/128])."""
+    return _quant_groups(w, (128, 128), _pow2_scale_from_amax)
 
 
 def quant_1x128(x):

@@ -131,3 +131,59 @@ def test_block_size_trend_from_page():
     assert errs[-1] < errs[0] and errs[2] < errs[0]
     assert dead[0] > dead[2] >= dead[3]
     assert g["dead"][0] > g["dead"][2] > g["dead"][3]
+
+
+# ---- power-of-two scales (the MX-native variant) ---------------------------------------
+
+def _blocks_with_amax(amaxes, seed=0):
+    """One 1x128 tile per amax value, random contents scaled so the tile's max-abs is it."""
+    rng = np.random.default_rng(seed)
+    x = rng.uniform(-1, 1, (len(amaxes), 128)).astype(np.float64)
+    x[:, 0] = 1.0
+    return (x * np.asarray(amaxes, np.float64)[:, None]).astype(np.float32)
+
+
+def test_pow2_scale_is_the_smallest_power_of_two_that_fits():
+    amaxes = [3.0, 448.0, 448.0 * 2 ** -20, 1e-30, 12345.0, 0.5, 224.0, 224.0001, 1.0]
+    x = _blocks_with_amax(amaxes)
+    q, s = oracle.quant_1x128_pow2(x)
+    s = s[0].astype(np.float64)
+    amax = np.abs(x.astype(np.float64)).max(axis=1)
+    mant, _ = np.frexp(s)
+    assert (mant == 0.5).all()                                # powers of two
+    assert (amax / s <= 448).all() and (amax / s > 224).all()  # the smallest that fits
+    dec = oracle.e4m3_decode(q)
+    assert np.abs(dec).max() <= 448                           # never saturates
+
+
+def test_pow2_closed_form_and_zero_tile():
+    # amax 3 -> 448 * 2^-8 = 1.75 < 3 <= 448 * 2^-7 = 3.5, so s = 2^-7 and 3 / s = 384,
+    # which E4M3 holds exactly (1.5 * 2^8)
+    x = np.zeros((2, 128), np.float32)
+    x[0, 5] = 3.0
+    x[0, 6] = -1.5
+    q, s = oracle.quant_1x128_pow2(x)
+    assert s[0, 0] == 2.0 ** -7 and s[0, 1] == 1.0
+    dec = oracle.e4m3_decode(q)
+    assert dec[0, 5] == 384.0 and dec[0, 6] == -192.0
+    assert (q[1] == 0).all()
+
+
+def test_pow2_equals_fp32_scales_when_amax_over_448_is_a_power_of_two():
+    amaxes = [448.0 * 2.0 ** k for k in range(-12, 6)]
+    x = _blocks_with_amax(amaxes, seed=3)
+    q2, s2 = oracle.quant_1x128_pow2(x)
+    q1, s1 = oracle.quant_1x128(x)
+    assert np.array_equal(s1, s2) and np.array_equal(q1, q2)
+
+
+def test_pow2_reconstruction_error_bound_and_weight_blocks():
+    rng = np.random.default_rng(8)
+    w = (rng.standard_normal((256, 384)) * np.exp(rng.uniform(-6, 6, (256, 1)))).astype(np.float32)
+    q, s = oracle.quant_128x128_pow2(w)
+    assert s.shape == (2, 3)
+    assert (np.frexp(s.astype(np.float64))[0] == 0.5).all()
+    w_hat = oracle.dequant_128x128(q, s)
+    full = np.repeat(np.repeat(s.astype(np.float64), 128, 0), 128, 1)
+    # half an E4M3 ulp (3 fraction bits) relative, or half the subnormal unit 2^-9
+    assert (np.abs(w_hat - w) <= 2.0 ** -4 * np.abs(w) + full * 2.0 ** -10).all()
