@@ -1,7 +1,7 @@
 """Benchmark of the MoE FFN layer forward (DeepSeek-V3 shape) on B300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--config v3|decode|skewed|tiny|sweep]
+                    [--config v3|decode|skewed|tiny|sweep|sweep_mx]
 
 One step is one pass of the whole hot path over one batch: router logits, routing,
 permutation, 1x128 quantisation, row gather, gate/up grouped GEMM with fused SwiGLU and
@@ -51,7 +51,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", choices=["v3", "decode", "skewed", "tiny", "v3_e32", "sweep"],
+    ap.add_argument("--config", choices=["v3", "decode", "skewed", "tiny", "v3_e32", "sweep",
+                                         "sweep_mx"],
                     default="v3")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -508,21 +509,25 @@ def main_reference(args, cfg, rank, world, dev):
     print(json.dumps(out), flush=True)
 
 
-def main_sweep(args, rank, dev):
+def main_sweep(args, rank, dev, mx=False):
     """Standalone FP8 block-scaled GEMM sweep (one JSON line per shape); L2 is flushed
-    between timed launches."""
+    between timed launches.  mx: the MX-native variant (power-of-two scales applied by
+    the tensor core) on the same inputs quantised with power-of-two scales."""
     from fp8_block_scaled_bias_b300 import ops
     pk = peaks()
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     for (M, N, K) in workloads.GEMM_SWEEP:
         a = workloads.gen_normal(M, K, sub_seed=31, device="cuda").to(torch.bfloat16)
         b = workloads.gen_normal(N, K, sub_seed=32, device="cuda")
-        qa, sa = ops.quant_1x128(a)
-        qb, sb = ops.quant_128x128(b)
+        qa, sa = ops.quant_1x128(a, pow2=mx)
+        qb, sb = ops.quant_128x128(b, pow2=mx)
         del a, b
         seg = torch.tensor([0, M], dtype=torch.int32, device=dev)
         C = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
-        run = lambda: ops.grouped_gemm(qa, sa, qb[None], sb[None], seg, M, out=C)
+        if mx:
+            run = lambda: ops.mx_grouped_gemm(qa, sa, qb[None], sb[None], seg, M, out=C)
+        else:
+            run = lambda: ops.grouped_gemm(qa, sa, qb[None], sb[None], seg, M, out=C)
         for _ in range(args.warmup):
             run()
         ts = []
@@ -538,7 +543,8 @@ def main_sweep(args, rank, dev):
         ms = statistics.median(e0.elapsed_time(e1) for e0, e1 in ts)
         tf = 2.0 * M * N * K / (ms / 1e3) / 1e12
         fp8_peak = 2.0 * pk["bf16_tflops"]
-        print(json.dumps({"metric": "FP8 block-scaled GEMM TFLOPS", "value": round(tf, 1),
+        name = "FP8 MX-scaled GEMM TFLOPS" if mx else "FP8 block-scaled GEMM TFLOPS"
+        print(json.dumps({"metric": name, "value": round(tf, 1),
                           "unit": "TFLOP/s", "config": {"workload": f"GEMM sweep M={M} N={N} K={K}",
                                                         "l2": "flushed between launches"},
                           "ms": round(ms, 4), "steps": args.steps,
@@ -555,7 +561,7 @@ def main():
         rank = int(os.environ.get("RANK", "0"))
         if rank != 0:
             return
-        cfg = workloads.CONFIGS["v3" if args.config in ("sweep",) else args.config]
+        cfg = workloads.CONFIGS["v3" if args.config in ("sweep", "sweep_mx") else args.config]
         torch.cuda.set_device(0)
         main_reference(args, cfg, 0, 1, torch.device("cuda", 0))
         return
@@ -565,8 +571,8 @@ def main():
         from fp8_block_scaled_bias_b300.build import build
         build()
     pkg.load()
-    if args.config == "sweep":
-        main_sweep(args, rank, dev)
+    if args.config in ("sweep", "sweep_mx"):
+        main_sweep(args, rank, dev, mx=args.config == "sweep_mx")
     else:
         main_ours(args, workloads.CONFIGS[args.config], rank, world, dev)
     if world > 1:

@@ -119,14 +119,24 @@ int moe_permute_noalloc(const int32_t* topk_idx, int T, int K, int E, int includ
 
 // ---- quantisation --------------------------------------------------------------------
 
-int fp8_quant_1x128(const uint16_t* x, int rows, int cols, int ldx, uint8_t* q, float* scale,
-                    void* stream) {
+static int quant_1x128_common(const uint16_t* x, int rows, int cols, int ldx, uint8_t* q,
+                              float* scale, bool pow2, void* stream) {
   if (rows < 0 || cols < 0 || cols % 128 != 0 || ldx < cols || ldx % 8 != 0)
     return MOE_ERR_INVALID_ARG;
   if (rows == 0 || cols == 0) return MOE_OK;
   if (!x || !q || !scale || !aligned16(x) || (reinterpret_cast<uintptr_t>(q) & 7u))
     return MOE_ERR_INVALID_ARG;
-  return moe::launch_quant_1x128(x, rows, cols, ldx, q, scale, as_stream(stream));
+  return moe::launch_quant_1x128(x, rows, cols, ldx, q, scale, pow2, as_stream(stream));
+}
+
+int fp8_quant_1x128(const uint16_t* x, int rows, int cols, int ldx, uint8_t* q, float* scale,
+                    void* stream) {
+  return quant_1x128_common(x, rows, cols, ldx, q, scale, false, stream);
+}
+
+int fp8_quant_1x128_pow2(const uint16_t* x, int rows, int cols, int ldx, uint8_t* q,
+                         float* scale, void* stream) {
+  return quant_1x128_common(x, rows, cols, ldx, q, scale, true, stream);
 }
 
 int fp8_quant_scatter_1x128(const uint16_t* x, int T, int cols, int ldx, const int32_t* row_of,
@@ -142,13 +152,23 @@ int fp8_quant_scatter_1x128(const uint16_t* x, int T, int cols, int ldx, const i
                                          scale, dev_status, as_stream(stream));
 }
 
-int fp8_quant_128x128(const float* w, int rows, int cols, uint8_t* q, float* scale,
-                      void* stream) {
+static int quant_128x128_common(const float* w, int rows, int cols, uint8_t* q, float* scale,
+                                bool pow2, void* stream) {
   if (rows < 0 || cols < 0 || rows % 128 != 0 || cols % 128 != 0) return MOE_ERR_INVALID_ARG;
   if (rows == 0 || cols == 0) return MOE_OK;
   if (!w || !q || !scale || !aligned16(w) || (reinterpret_cast<uintptr_t>(q) & 3u))
     return MOE_ERR_INVALID_ARG;
-  return moe::launch_quant_128x128(w, rows, cols, q, scale, as_stream(stream));
+  return moe::launch_quant_128x128(w, rows, cols, q, scale, pow2, as_stream(stream));
+}
+
+int fp8_quant_128x128(const float* w, int rows, int cols, uint8_t* q, float* scale,
+                      void* stream) {
+  return quant_128x128_common(w, rows, cols, q, scale, false, stream);
+}
+
+int fp8_quant_128x128_pow2(const float* w, int rows, int cols, uint8_t* q, float* scale,
+                           void* stream) {
+  return quant_128x128_common(w, rows, cols, q, scale, true, stream);
 }
 
 // ---- grouped GEMM --------------------------------------------------------------------
@@ -164,6 +184,19 @@ static int check_gemm_dims(int G, int M, int N, int K) {
   if (G > 1024) return MOE_ERR_UNSUPPORTED;
   if (static_cast<long long>(G) * N > INT32_MAX || K > (1 << 24)) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
+}
+
+int fp8_mx_grouped_gemm(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
+                        const int32_t* seg_offsets, int G, int M, int N, int K, uint16_t* C,
+                        int ldc, int32_t* dev_status, void* stream) {
+  const int st = check_gemm_dims(G, M, N, K);
+  if (st != MOE_OK) return st;
+  if (M == 0) return MOE_OK;
+  if (!A || !sA || !B || !sB || !seg_offsets || !C) return MOE_ERR_INVALID_ARG;
+  if (ldc < N || ldc % 8 != 0 || !aligned16(A) || !aligned16(B) || !aligned16(C))
+    return MOE_ERR_INVALID_ARG;
+  return moe::launch_mx_gemm(A, sA, B, sB, seg_offsets, G, M, N, K, C, ldc, dev_status,
+                             as_stream(stream));
 }
 
 int fp8_blockscaled_grouped_gemm(const uint8_t* A, const float* sA, int M_a,

@@ -1,0 +1,435 @@
+// MX-native variant of the grouped FP8 GEMM: the block scales are applied by the tensor
+// core itself (tcgen05.mma kind::mxf8f6f4 with UE8M0 scale factors), so the FP32
+// accumulator stays in TMEM for the whole K loop and there is no per-K-block
+// promotion round trip.
+//
+//   C[r][n] = sum_kb sA[kb][r] * sB[g][n/128][kb] * P_kb[r][n]      (same formula as the
+//                                                                    FP32-scale GEMM)
+// with every scale a power of two.  The pages note that V3's 1x128 / 128x128 groups match
+// the microscaling formats Blackwell tensor cores take natively ("DeepSeek-V3" summary,
+// core idea 6(a)) and ask for native group-scaled MMA (core idea 8, hardware wishlist).
+// The hardware scale block is 32 deep along K, so the four 32-deep steps of a 128-deep
+// block read the same scale.
+//
+// Kernel shape (one CTA per SM, persistent):
+//   warp 0       TMA producer: A tile 128x128 and B tile 256x128 (FP8) per K block
+//   warp 1       TMEM allocation; one thread issues 4 block-scaled MMAs (M128 N256 K32)
+//                per K block into the one accumulator; never touches shared memory in
+//                its loop (a named barrier with the scheduler releases it)
+//   warps 2-5    scale writers: per K block, the exponent bytes of the tile's 128 row
+//                scales and 256 column scales go into a ring of TMEM scale slots
+//                (tcgen05.st; one warp per TMEM lane quarter, all four write the same
+//                words, so each quarter holds a full copy)
+//   warps 6-13   epilogue: TMEM accumulator -> BF16 C, then release the accumulator
+//   warp 14      scheduler: waits for the stage, the scale slot and (at a tile's first
+//                K block) the accumulator, then releases warp 1
+// TMEM: columns [0, 256) accumulator; scale slot j at 256 + 16 j: 4 columns of row scales
+// (word (lane l, column c) = rows l % 32 + 32 c, the byte repeated for the four 32-deep
+// steps), then 8 columns of column scales laid out the same way for 256 B rows.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace moe {
+
+namespace mx {
+constexpr int BM = 128, BN = 256, BK = 128;
+constexpr int A_BYTES = BM * BK;
+constexpr int B_BYTES = BN * BK;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int STAGES = 4;
+constexpr int SF_SLOTS = 4;
+constexpr int SF_WARP0 = 2, SF_WARPS = 4;
+constexpr int EPI_WARP0 = 6, EPI_WARPS = 8;
+constexpr int SCHED_WARP = 14;
+constexpr int THREADS = 15 * 32;
+constexpr int MMA_BAR = 1;
+constexpr int MAX_G = 1024;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t SF_COL0 = 256, SF_SLOT_COLS = 16, SFB_OFF = 4;
+
+constexpr int OFF_A = 0;
+constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+constexpr int OFF_BAR = OFF_B + STAGES * B_BYTES;
+// full[STAGES], empty[STAGES], sf_full[SF_SLOTS], sf_empty[SF_SLOTS], tfull, tempty, drain
+constexpr int NUM_BARS = 2 * STAGES + 2 * SF_SLOTS + 3;
+constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;   // tmem slot, abort, total, bad
+constexpr int OFF_SEG = OFF_MISC + 16;
+constexpr int OFF_USTART = OFF_SEG + (MAX_G + 1) * 4;
+constexpr int OFF_WSUM = OFF_USTART + (MAX_G + 1) * 4;
+constexpr int SMEM_USED = OFF_WSUM + 32 * 4;
+constexpr int SMEM_ALLOC = SMEM_USED + 1024;
+static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
+
+// Instruction descriptor of a block-scaled MMA (kind::mxf8f6f4; D is FP32): bits [4,6)
+// scale byte of B, [7,10) A type, [10,13) B type (0 = E4M3), [17,23) N >> 3, bit 23 scale
+// type (1 = UE8M0), [24,29) M >> 4, [29,31) scale byte of A.  The scale byte picks one of
+// the four bytes of each 32-bit scale word in TMEM.
+constexpr uint32_t idesc_mx(int M, int N, uint32_t a_byte, uint32_t b_byte) {
+  return (b_byte << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (1u << 23) | (static_cast<uint32_t>(M >> 4) << 24) | (a_byte << 29);
+}
+}  // namespace mx
+
+struct MxParams {
+  const float* sA;
+  const float* sB;
+  const int32_t* seg;
+  int G, M, N, K;
+  uint16_t* C;
+  int ldc;
+  int32_t* status;
+};
+
+namespace {
+
+MOE_DEV void mma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                    uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X "
+      "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+MOE_DEV void tmem_st_x4(uint32_t taddr, const uint32_t (&r)[4]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr),
+               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
+               : "memory");
+}
+
+MOE_DEV void tmem_st_x8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+               "r"(r[7])
+               : "memory");
+}
+
+MOE_DEV void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// A power-of-two FP32 scale as a UE8M0 byte repeated four times (one per 32-deep step).
+// Anything else (zero, subnormal, inf/NaN, a mantissa bit set) is a data error.
+MOE_DEV uint32_t ue8m0_word(float s, bool& bad) {
+  const uint32_t b = __float_as_uint(s);
+  const uint32_t e = (b >> 23) & 0xFFu;
+  if ((b & 0x807FFFFFu) != 0 || e == 0 || e == 0xFFu) bad = true;
+  return e * 0x01010101u;
+}
+
+MOE_DEV void decode_unit(int unit, const int* ustart, const int* seg, int G, int& g, int& m0,
+                         int& rows_valid, int& nt) {
+  int lo = 0, hi = G - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (ustart[mid] <= unit) lo = mid;
+    else hi = mid - 1;
+  }
+  g = lo;
+  const int cnt = seg[g + 1] - seg[g];
+  const int mt = (cnt + mx::BM - 1) / mx::BM;
+  const int local = unit - ustart[g];
+  m0 = seg[g] + (local % mt) * mx::BM;
+  nt = local / mt;
+  rows_valid = min(mx::BM, seg[g + 1] - m0);
+}
+
+MOE_DEV void mbar_drain_mx(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return;
+  }
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(mx::THREADS, 1)
+    fp8_mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                       const __grid_constant__ CUtensorMap tmB, const MxParams p) {
+  using namespace mx;
+  extern __shared__ uint8_t mx_smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(mx_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + OFF_BAR;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto sf_full_bar = [&](int j) { return bar0 + 8u * (2 * STAGES + j); };
+  auto sf_empty_bar = [&](int j) { return bar0 + 8u * (2 * STAGES + SF_SLOTS + j); };
+  const uint32_t tfull_bar = bar0 + 8u * (2 * STAGES + 2 * SF_SLOTS);
+  const uint32_t tempty_bar = tfull_bar + 8u;
+  const uint32_t drain_bar = tfull_bar + 16u;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
+  int* total_units = reinterpret_cast<int*>(smem + OFF_MISC + 8);
+  int* bad = reinterpret_cast<int*>(smem + OFF_MISC + 12);
+  int* seg = reinterpret_cast<int*>(smem + OFF_SEG);
+  int* ustart = reinterpret_cast<int*>(smem + OFF_USTART);
+  int* wsum = reinterpret_cast<int*>(smem + OFF_WSUM);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = p.G;
+  const int NT = (p.N + BN - 1) / BN;        // N tiles (the last may be half-filled)
+  const int NB = p.N / 128;                  // weight-scale rows per segment
+  const int KB = p.K / BK;
+
+  // ---- segment table and unit prefix ----
+  if (tid == 0) { *abort_flag = 0; *bad = 0; }
+  for (int i = tid; i <= G; i += THREADS) seg[i] = p.seg[i];
+  __syncthreads();
+  {
+    const int per = (G + THREADS - 1) / THREADS;
+    const int g0 = min(G, tid * per), g1 = min(G, g0 + per);
+    int local = 0;
+    for (int g = g0; g < g1; ++g) {
+      const int cnt = seg[g + 1] - seg[g];
+      if (cnt < 0) *bad = 1;
+      local += (max(cnt, 0) + BM - 1) / BM * NT;
+    }
+    if (tid == 0 && (seg[0] != 0 || seg[G] > p.M)) *bad = 1;
+    int incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+      if (lane >= off) incl += o;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    int wbase = 0;
+    for (int w = 0; w < warp; ++w) wbase += wsum[w];
+    int run = wbase + incl - local;
+    for (int g = g0; g < g1; ++g) {
+      ustart[g] = run;
+      run += (max(seg[g + 1] - seg[g], 0) + BM - 1) / BM * NT;
+    }
+    if (tid == THREADS - 1) {
+      int tot = 0;
+      for (int w = 0; w < THREADS / 32; ++w) tot += wsum[w];
+      *total_units = tot;
+      ustart[G] = tot;
+    }
+  }
+  __syncthreads();
+  if (*bad) {
+    if (tid == 0) set_status(p.status, MOE_ERR_DEVICE_DATA);
+    return;
+  }
+  const int total = *total_units;
+
+  if (tid == 0) {
+    for (int s = 0; s < STAGES; ++s) { mbar_init(full_bar(s), 1); mbar_init(empty_bar(s), 1); }
+    for (int j = 0; j < SF_SLOTS; ++j) {
+      mbar_init(sf_full_bar(j), SF_WARPS);
+      mbar_init(sf_empty_bar(j), 1);
+    }
+    mbar_init(tfull_bar, 1);
+    mbar_init(tempty_bar, EPI_WARPS);
+    mbar_init(drain_bar, 1);
+    fence_barrier_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int first_unit = blockIdx.x, unit_stride = gridDim.x;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int unit = first_unit; ok && unit < total; unit += unit_stride) {
+        int g, m0, rv, nt;
+        decode_unit(unit, ustart, seg, G, g, m0, rv, nt);
+        const int brow = g * p.N + nt * BN;
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (!mbar_wait(empty_bar(s), ph ^ 1, abort_flag, p.status)) { ok = false; break; }
+          mbar_arrive_expect_tx(full_bar(s), STAGE_BYTES);
+          tma_load_2d(sbase + OFF_A + s * A_BYTES, &tmA, kb * BK, m0, full_bar(s));
+          tma_load_2d(sbase + OFF_B + s * B_BYTES, &tmB, kb * BK, brow, full_bar(s));
+        }
+      }
+      if (!ok) {
+        const uint32_t first = it > STAGES ? it - STAGES : 0;
+        for (uint32_t i = first; i < it; ++i) mbar_drain_mx(full_bar(i % STAGES), (i / STAGES) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    uint32_t it = 0;
+    bool ok = true;
+    for (int unit = first_unit; ok && unit < total; unit += unit_stride) {
+      for (int kb = 0; kb < KB; ++kb, ++it) {
+        if (named_bar_sync_or(MMA_BAR, 64, false)) { ok = false; break; }
+        if (lane == 0) {
+          const int s = it % STAGES;
+          const int j = it % SF_SLOTS;
+          tc_fence_after();
+          const uint64_t adesc = smem_desc_sw128(sbase + OFF_A + s * A_BYTES);
+          const uint64_t bdesc = smem_desc_sw128(sbase + OFF_B + s * B_BYTES);
+          const uint32_t sfa = tmem_base + SF_COL0 + j * SF_SLOT_COLS;
+#pragma unroll
+          for (int k = 0; k < BK / 32; ++k)
+            mma_mx(tmem_base, adesc + 2 * k, bdesc + 2 * k, idesc_mx(BM, BN, k, k), sfa,
+                   sfa + SFB_OFF, (kb > 0 || k > 0) ? 1u : 0u);
+          mma_commit(empty_bar(s));
+          mma_commit(sf_empty_bar(j));
+          if (kb == KB - 1) mma_commit(tfull_bar);
+        }
+        __syncwarp();
+      }
+    }
+    if (lane == 0) {
+      mma_commit(drain_bar);
+      mbar_drain_mx(drain_bar, 0);
+    }
+    __syncwarp();
+  } else if (warp == SCHED_WARP) {
+    // ---------------- MMA scheduler ----------------
+    uint32_t it = 0, tt = 0;
+    bool ok = true;
+    for (int unit = first_unit; ok && unit < total; unit += unit_stride, ++tt) {
+      for (int kb = 0; kb < KB; ++kb, ++it) {
+        int good = 1;
+        if (lane == 0) {
+          const int s = it % STAGES;
+          const int j = it % SF_SLOTS;
+          good = (kb != 0 || mbar_wait(tempty_bar, (tt & 1) ^ 1, abort_flag, p.status)) &&
+                 mbar_wait(sf_full_bar(j), (it / SF_SLOTS) & 1, abort_flag, p.status) &&
+                 mbar_wait(full_bar(s), (it / STAGES) & 1, abort_flag, p.status);
+        }
+        good = __shfl_sync(0xFFFFFFFFu, good, 0);
+        tc_fence_before();
+        if (named_bar_sync_or(MMA_BAR, 64, good == 0)) { ok = false; break; }
+      }
+    }
+  } else if (warp >= SF_WARP0 && warp < SF_WARP0 + SF_WARPS) {
+    // ---------------- scale writers ----------------
+    const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    uint32_t it = 0;
+    bool ok = true, badscale = false;
+    for (int unit = first_unit; ok && unit < total; unit += unit_stride) {
+      int g, m0, rv, nt;
+      decode_unit(unit, ustart, seg, G, g, m0, rv, nt);
+      const int nb0 = 2 * nt, nb1 = min(2 * nt + 1, NB - 1);
+      const float* sbg = p.sB + static_cast<long long>(g) * NB * KB;
+      for (int kb = 0; kb < KB; ++kb, ++it) {
+        const int j = it % SF_SLOTS;
+        if (!mbar_wait_warp(sf_empty_bar(j), ((it / SF_SLOTS) & 1) ^ 1, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t wa[4], wb[8];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int r = min(m0 + lane + 32 * c, p.M - 1);
+          wa[c] = ue8m0_word(__ldg(p.sA + static_cast<long long>(kb) * p.M + r), badscale);
+        }
+        const uint32_t b0 = ue8m0_word(__ldg(sbg + static_cast<long long>(nb0) * KB + kb), badscale);
+        const uint32_t b1 = ue8m0_word(__ldg(sbg + static_cast<long long>(nb1) * KB + kb), badscale);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) wb[c] = c < 4 ? b0 : b1;
+        const uint32_t col = tmem_base + lane_addr + SF_COL0 + j * SF_SLOT_COLS;
+        tmem_st_x4(col, wa);
+        tmem_st_x8(col + SFB_OFF, wb);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sf_full_bar(j));
+      }
+    }
+    if (__any_sync(0xFFFFFFFFu, badscale) && lane == 0) set_status(p.status, MOE_ERR_DEVICE_DATA);
+  } else if (warp >= EPI_WARP0 && warp < EPI_WARP0 + EPI_WARPS) {
+    // ---------------- epilogue: accumulator -> BF16 ----------------
+    const int q = warp & 3;
+    const int grp = (warp - EPI_WARP0) >> 2;
+    const int row = q * 32 + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
+    uint32_t tt = 0;
+    for (int unit = first_unit; unit < total; unit += unit_stride, ++tt) {
+      int g, m0, rv, nt;
+      decode_unit(unit, ustart, seg, G, g, m0, rv, nt);
+      if (!mbar_wait_warp(tfull_bar, tt & 1, abort_flag, p.status)) break;
+      tc_fence_after();
+      const int col0 = nt * BN + grp * 128;
+      const bool store = row < rv && col0 < p.N;
+      uint4* dst = reinterpret_cast<uint4*>(p.C + static_cast<long long>(m0 + row) * p.ldc + col0);
+#pragma unroll
+      for (int c = 0; c < 8; c += 2) {
+        uint32_t v[2][16];
+        const uint32_t ta = tmem_base + lane_addr + static_cast<uint32_t>(grp * 128 + c * 16);
+        tmem_ld_32x32b_x16(ta, v[0]);
+        tmem_ld_32x32b_x16(ta + 16, v[1]);
+        tmem_ld_wait();
+        if (store) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              uint4 o;
+              o.x = pack_bf16x2(__uint_as_float(v[h][8 * i + 0]), __uint_as_float(v[h][8 * i + 1]));
+              o.y = pack_bf16x2(__uint_as_float(v[h][8 * i + 2]), __uint_as_float(v[h][8 * i + 3]));
+              o.z = pack_bf16x2(__uint_as_float(v[h][8 * i + 4]), __uint_as_float(v[h][8 * i + 5]));
+              o.w = pack_bf16x2(__uint_as_float(v[h][8 * i + 6]), __uint_as_float(v[h][8 * i + 7]));
+              dst[(c + h) * 2 + i] = o;
+            }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ---- host side ------------------------------------------------------------------------
+
+bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* ptr,
+                    uint64_t inner, uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
+                    uint32_t box_outer);   // runtime.cu
+
+int launch_mx_gemm(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
+                   const int32_t* seg, int G, int M, int N, int K, uint16_t* C, int ldc,
+                   int32_t* status, cudaStream_t stream) {
+  using namespace mx;
+  if (M == 0) return MOE_OK;
+  CUtensorMap tmA, tmB;
+  if (!encode_tmap_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, K, BK, BM)) return MOE_ERR_CUDA;
+  if (!encode_tmap_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, static_cast<uint64_t>(G) * N, K,
+                      BK, BN))
+    return MOE_ERR_CUDA;
+  MxParams p;
+  p.sA = sA; p.sB = sB; p.seg = seg;
+  p.G = G; p.M = M; p.N = N; p.K = K;
+  p.C = C; p.ldc = ldc; p.status = status;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(fp8_mx_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SMEM_ALLOC) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    attr_set = true;
+  }
+  const long long units = (static_cast<long long>(M) / BM + G) * ((N + BN - 1) / BN);
+  long long grid = num_sms();
+  if (units < grid) grid = units;
+  if (grid < 1) grid = 1;
+  fp8_mx_gemm_kernel<<<static_cast<unsigned>(grid), THREADS, SMEM_ALLOC, stream>>>(tmA, tmB, p);
+  return check_launch();
+}
+
+}  // namespace moe

@@ -10,8 +10,32 @@
 
 namespace moe {
 
+namespace {
+// Power-of-two scale rule (the MX-native variant): the smallest s = 2^k with 448 * s >= amax,
+// found exactly from amax's exponent and mantissa (448 = 1.75 * 2^8), at least 2^-126;
+// s = 1 for amax == 0.  Division by it is exact.
+MOE_DEV float pow2_scale_from_amax(float amax) {
+  if (amax == 0.0f) return 1.0f;
+  uint32_t b = __float_as_uint(amax);
+  int e = static_cast<int>((b >> 23) & 0xFFu) - 127;
+  if (((b >> 23) & 0xFFu) == 0) {                         // subnormal amax: rescale exactly
+    b = __float_as_uint(amax * 18446744073709551616.0f);  // * 2^64
+    e = static_cast<int>((b >> 23) & 0xFFu) - 127 - 64;
+  }
+  int k = e - 8 + ((b & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+  k = max(k, -126);
+  return __uint_as_float(static_cast<uint32_t>(k + 127) << 23);
+}
+
+template <bool POW2>
+MOE_DEV float scale_rule(float amax) {
+  return POW2 ? pow2_scale_from_amax(amax) : e4m3_scale_from_amax(amax);
+}
+}  // namespace
+
 // Half a warp per 1x128 tile: 16 lanes x 8 BF16 values.  Tiles are numbered with the
 // column block fastest so a warp reads 512 contiguous bytes of one row.
+template <bool POW2>
 __global__ void __launch_bounds__(256) quant_1x128_kernel(const uint16_t* __restrict__ x,
                                                            int rows, int ncb, int ldx,
                                                            uint8_t* __restrict__ q,
@@ -44,7 +68,7 @@ __global__ void __launch_bounds__(256) quant_1x128_kernel(const uint16_t* __rest
 #pragma unroll
     for (int off = 8; off > 0; off >>= 1)
       amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
-    const float s = e4m3_scale_from_amax(amax);
+    const float s = scale_rule<POW2>(amax);
     uint32_t out[2];
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
@@ -129,6 +153,7 @@ int launch_quant_scatter_1x128(const uint16_t* x, int T, int cols, int ldx, cons
 }
 
 // One block per 128x128 weight block; thread t covers row t/2, 64 columns.
+template <bool POW2>
 __global__ void __launch_bounds__(256) quant_128x128_kernel(const float* __restrict__ w,
                                                              int rows, int cols,
                                                              uint8_t* __restrict__ q,
@@ -151,7 +176,7 @@ __global__ void __launch_bounds__(256) quant_128x128_kernel(const float* __restr
   amax = wmax[0];
 #pragma unroll
   for (int i = 1; i < 8; ++i) amax = fmaxf(amax, wmax[i]);
-  const float s = e4m3_scale_from_amax(amax);
+  const float s = scale_rule<POW2>(amax);
   uint8_t* dst = q + static_cast<long long>(r) * cols + c0;
   for (int i = 0; i < 64; i += 4) {
     const float4 v = *reinterpret_cast<const float4*>(src + i);
@@ -163,23 +188,30 @@ __global__ void __launch_bounds__(256) quant_128x128_kernel(const float* __restr
 }
 
 int launch_quant_1x128(const uint16_t* x, int rows, int cols, int ldx, uint8_t* q,
-                       float* scale, cudaStream_t stream) {
+                       float* scale, bool pow2, cudaStream_t stream) {
   const long long ntiles = static_cast<long long>(rows) * (cols / 128);
   if (ntiles == 0) return MOE_OK;
   const long long pairs = (ntiles + 1) / 2;
   long long blocks = (pairs + 7) / 8;                 // 8 warps per block
   const long long cap = static_cast<long long>(num_sms()) * 16;
   if (blocks > cap) blocks = cap;
-  quant_1x128_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(x, rows, cols / 128, ldx,
-                                                                        q, scale, ntiles);
+  if (pow2)
+    quant_1x128_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        x, rows, cols / 128, ldx, q, scale, ntiles);
+  else
+    quant_1x128_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        x, rows, cols / 128, ldx, q, scale, ntiles);
   return check_launch();
 }
 
 int launch_quant_128x128(const float* w, int rows, int cols, uint8_t* q, float* scale,
-                         cudaStream_t stream) {
+                         bool pow2, cudaStream_t stream) {
   if (rows == 0 || cols == 0) return MOE_OK;
   dim3 grid(cols / 128, rows / 128);
-  quant_128x128_kernel<<<grid, 256, 0, stream>>>(w, rows, cols, q, scale);
+  if (pow2)
+    quant_128x128_kernel<true><<<grid, 256, 0, stream>>>(w, rows, cols, q, scale);
+  else
+    quant_128x128_kernel<false><<<grid, 256, 0, stream>>>(w, rows, cols, q, scale);
   return check_launch();
 }
 

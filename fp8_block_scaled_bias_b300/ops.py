@@ -158,8 +158,9 @@ def permute(idx, E, include_shared=True, status=None, out=None):
 
 # ---- quantisation -----------------------------------------------------------------------
 
-def quant_1x128(x, out=None):
-    """BF16 [rows, cols] -> (E4M3 codes uint8 [rows, cols], scales FP32 [cols/128, rows])."""
+def quant_1x128(x, out=None, pow2=False):
+    """BF16 [rows, cols] -> (E4M3 codes uint8 [rows, cols], scales FP32 [cols/128, rows]);
+    pow2: power-of-two scales (the MX-native variant)."""
     _check(x, _BF16, "x", 2)
     rows, cols = x.shape
     if out is None:
@@ -167,7 +168,8 @@ def quant_1x128(x, out=None):
         s = torch.empty(cols // 128, rows, dtype=_F32, device=x.device)
     else:
         q, s = out
-    call("fp8_quant_1x128", _ptr(x), rows, cols, cols, _ptr(q), _ptr(s), _stream())
+    call("fp8_quant_1x128_pow2" if pow2 else "fp8_quant_1x128", _ptr(x), rows, cols, cols,
+         _ptr(q), _ptr(s), _stream())
     return q, s
 
 
@@ -190,13 +192,15 @@ def quant_scatter_1x128(x, row_of, n_rows, shared_row_base=None, status=None, ou
     return q, s
 
 
-def quant_128x128(w):
-    """FP32 [rows, cols] -> (E4M3 codes uint8, scales FP32 [rows/128, cols/128])."""
+def quant_128x128(w, pow2=False):
+    """FP32 [rows, cols] -> (E4M3 codes uint8, scales FP32 [rows/128, cols/128]); pow2:
+    power-of-two scales (the MX-native variant)."""
     _check(w, _F32, "w", 2)
     rows, cols = w.shape
     q = torch.empty(rows, cols, dtype=_U8, device=w.device)
     s = torch.empty(rows // 128, cols // 128, dtype=_F32, device=w.device)
-    call("fp8_quant_128x128", _ptr(w), rows, cols, _ptr(q), _ptr(s), _stream())
+    call("fp8_quant_128x128_pow2" if pow2 else "fp8_quant_128x128", _ptr(w), rows, cols,
+         _ptr(q), _ptr(s), _stream())
     return q, s
 
 
@@ -222,6 +226,21 @@ def grouped_gemm(A, sA, B, sB, seg_offsets, M, a_rows=None, status=None, out=Non
     call("fp8_blockscaled_grouped_gemm", _ptr(A), _ptr(sA), A.shape[0], _ptr(a_rows), _ptr(B),
          _ptr(sB), _ptr(seg_offsets), G, M, N, K, _ptr(C), C.stride(0), _ptr(status), ws, wsb,
          _stream())
+    return C
+
+
+def mx_grouped_gemm(A, sA, B, sB, seg_offsets, M, status=None, out=None):
+    """MX-native variant of grouped_gemm (power-of-two scales applied by the tensor core);
+    A rows already in segment order."""
+    _check(A, _U8, "A", 2)
+    _check(sA, _F32, "sA", 2)
+    _check(B, _U8, "B", 3)
+    _check(sB, _F32, "sB", 3)
+    _check(seg_offsets, _I32, "seg_offsets", 1)
+    G, N, K = B.shape
+    C = out if out is not None else torch.empty(M, N, dtype=_BF16, device=A.device)
+    call("fp8_mx_grouped_gemm", _ptr(A), _ptr(sA), _ptr(B), _ptr(sB), _ptr(seg_offsets), G, M,
+         N, K, _ptr(C), C.stride(0), _ptr(status), _stream())
     return C
 
 

@@ -176,6 +176,17 @@ int fp8_quant_scatter_1x128(const uint16_t* x, int T, int cols, int ldx, const i
 int fp8_quant_128x128(const float* w, int rows, int cols, uint8_t* q, float* scale,
                       void* stream);
 
+/* Power-of-two-scale quantisers (the MX-native variant, for fp8_mx_grouped_gemm): the
+ * same tiles, layouts and E4M3 rounding, with s = the smallest power of two such that
+ * 448 * s >= amax (at least 2^-126; s = 1 when amax == 0), so x / s is exact and never
+ * saturates.  The pages note that the 1x128 / 128x128 groups match the microscaling
+ * formats Blackwell tensor cores take natively ([sum] core idea 6(a)) and mention
+ * power-of-two scales ([book] ch. 17 "Attention-related saved activations"). */
+int fp8_quant_1x128_pow2(const uint16_t* x, int rows, int cols, int ldx, uint8_t* q,
+                         float* scale, void* stream);
+int fp8_quant_128x128_pow2(const float* w, int rows, int cols, uint8_t* q, float* scale,
+                           void* stream);
+
 /* ---- FP8 block-scaled grouped GEMM ------------------------------------------------- */
 
 /* C[r][n] = sum_kb sA[kb][r'] * sB[g][n/128][kb] * sum_{k in kb} A[r'][k] * B[g][n][k]
@@ -197,6 +208,17 @@ int fp8_blockscaled_grouped_gemm(const uint8_t* A, const float* sA, int M_a,
                                  uint16_t* C, int ldc, int32_t* dev_status,
                                  void* ws, size_t ws_bytes, void* stream);
 size_t fp8_grouped_gemm_ws_bytes(int M, int K, int has_a_rows);
+
+/* MX-native variant ([sum] core idea 6(a), core idea 8 "native group-scaled MMA"): the
+ * same C as fp8_blockscaled_grouped_gemm (A rows in segment order, no a_rows) when every
+ * scale is a power of two, with the scales applied inside the tensor core
+ * (tcgen05.mma kind::mxf8f6f4, UE8M0 scale factors) and one FP32 accumulator per tile
+ * for the whole K loop: no per-block promotion.  Scales must be positive normal powers
+ * of two (fp8_quant_*_pow2); anything else sets MOE_ERR_DEVICE_DATA.  Same layouts and
+ * limits as fp8_blockscaled_grouped_gemm; no workspace. */
+int fp8_mx_grouped_gemm(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
+                        const int32_t* seg_offsets, int G, int M, int N, int K, uint16_t* C,
+                        int ldc, int32_t* dev_status, void* stream);
 
 /* ---- experts ----------------------------------------------------------------------- */
 

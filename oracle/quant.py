@@ -27,7 +27,8 @@ groups match the microscaling formats Blackwell tensor cores take natively ("Dee
 summary, core idea 6(a)), list native group-scaled MMA on the hardware wishlist (core
 idea 8), and mention power-of-two scales as a way to avoid extra quantisation error
 (DeepSeek-V3 book, ch. 17 "Attention-related saved activations").  Reading taken:
-  s = the smallest power of two with 448 * s >= amax   (s = 1 when amax == 0)
+  s = the smallest power of two with 448 * s >= amax, at least 2^-126 (the smallest
+      normal float32; s = 1 when amax == 0)
   q = E4M3_rne(x / s)        (the division is exact; |x / s| <= 448, so no saturation)
 with the same group shapes and layouts; the tensor core reads the scale's exponent byte.
 """
@@ -44,7 +45,8 @@ def _scale_from_amax(amax):
 
 
 def _pow2_scale_from_amax(amax):
-    """Smallest power of two s with 448 * s >= amax (exact comparisons); 1 for amax == 0."""
+    """Smallest power of two s >= 2^-126 with 448 * s >= amax (exact comparisons); 1 for
+    amax == 0."""
     amax = np.asarray(amax, dtype=np.float64)
     out = np.ones(amax.shape, dtype=np.float64)
     for i, a in np.ndenumerate(amax):
@@ -55,7 +57,7 @@ def _pow2_scale_from_amax(amax):
             e -= 1
         while E4M3_MAX * 2.0 ** e < a:                # step up until large enough
             e += 1
-        out[i] = 2.0 ** e
+        out[i] = 2.0 ** max(e, -126)                  # kept a normal float32
     return out.astype(np.float32)
 
 
