@@ -105,7 +105,9 @@ struct GemmParams {
 
 namespace {
 
-MOE_DEV float silu_f32(float g) { return __fdiv_rn(g, 1.0f + expf(-g)); }
+// silu on the tile-end critical path: the fast exponential and division (a few ulps;
+// h is compared with the oracle's float64 silu within a tolerance, never bit for bit)
+MOE_DEV float silu_f32(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 // Cluster work unit -> (segment, first row, valid rows, unit index within the row
 // block).  ustart[g] = first unit of segment g (non-decreasing); the largest g with
@@ -136,9 +138,12 @@ MOE_DEV void mbar_drain(uint32_t bar, uint32_t parity) {
   }
 }
 
-MOE_DEV uint32_t e4m3x4(float a, float b, float c, float d, float s) {
-  const uint32_t lo = f32x2_to_e4m3x2(__fdiv_rn(a, s), __fdiv_rn(b, s));
-  const uint32_t hi = f32x2_to_e4m3x2(__fdiv_rn(c, s), __fdiv_rn(d, s));
+// h requantisation: multiply by the correctly rounded reciprocal of the group scale (one
+// rounding more than x / s; it can move a code only when x / s sits within an FP32 ulp of
+// an E4M3 rounding boundary, and h itself carries the GEMM's FP32 rounding anyway)
+MOE_DEV uint32_t e4m3x4(float a, float b, float c, float d, float rs) {
+  const uint32_t lo = f32x2_to_e4m3x2(__fmul_rn(a, rs), __fmul_rn(b, rs));
+  const uint32_t hi = f32x2_to_e4m3x2(__fmul_rn(c, rs), __fmul_rn(d, rs));
   return lo | (hi << 16);
 }
 
@@ -485,6 +490,7 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
           if (!mbar_wait_warp(amax_bar(buf), (ucount >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
           amax = fmaxf(amax, amax_x[(buf * 2 + (grp ^ 1)) * BM + row]);
           const float s = e4m3_scale_from_amax(amax);
+          const float rs = __frcp_rn(s);
           if (row < rv) {
             const int f = p.N / 2;
             uint4* dst = reinterpret_cast<uint4*>(p.hq + static_cast<long long>(m0 + row) * f +
@@ -492,10 +498,10 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               const float* h = acc + 16 * j;
-              dst[j] = make_uint4(e4m3x4(h[0], h[1], h[2], h[3], s),
-                                  e4m3x4(h[4], h[5], h[6], h[7], s),
-                                  e4m3x4(h[8], h[9], h[10], h[11], s),
-                                  e4m3x4(h[12], h[13], h[14], h[15], s));
+              dst[j] = make_uint4(e4m3x4(h[0], h[1], h[2], h[3], rs),
+                                  e4m3x4(h[4], h[5], h[6], h[7], rs),
+                                  e4m3x4(h[8], h[9], h[10], h[11], rs),
+                                  e4m3x4(h[12], h[13], h[14], h[15], rs));
             }
             if (grp == 0) p.sh[static_cast<long long>(nt) * p.M + m0 + row] = s;
           }

@@ -66,7 +66,7 @@ static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 // scale byte of B, [7,10) A type, [10,13) B type (0 = E4M3), [17,23) N >> 3, bit 23 scale
 // type (1 = UE8M0), [24,29) M >> 4, [29,31) scale byte of A.  The scale byte picks one of
 // the four bytes of each 32-bit scale word in TMEM.
-constexpr uint32_t idesc_mx(int M, int N, uint32_t a_byte, uint32_t b_byte) {
+__host__ __device__ constexpr uint32_t idesc_mx(int M, int N, uint32_t a_byte, uint32_t b_byte) {
   return (b_byte << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
          (1u << 23) | (static_cast<uint32_t>(M >> 4) << 24) | (a_byte << 29);
 }
@@ -109,6 +109,7 @@ MOE_DEV void tmem_st_x8(uint32_t taddr, const uint32_t (&r)[8]) {
 }
 
 MOE_DEV void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 
 // A power-of-two FP32 scale as a UE8M0 byte repeated four times (one per 32-deep step).
 // Anything else (zero, subnormal, inf/NaN, a mantissa bit set) is a data error.
