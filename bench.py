@@ -80,12 +80,20 @@ def barrier(world):
 
 
 def max_over_ranks(v, world):
+    """The largest of the ranks' values (the slowest rank's time): one all-reduce on the
+    host-side timing result, not on the data path."""
     if world == 1:
         return v
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def weak_scaling_value(tokens_per_rank, steps, world, ms_max):
+    """Whole-job throughput: the tokens every rank processed over the slowest rank's time."""
+    return tokens_per_rank * world * steps / (ms_max / 1e3)
 
 
 # ---- peaks, clocks -----------------------------------------------------------------------
@@ -421,7 +429,7 @@ def main_ours(args, cfg, rank, world, dev):
     T, K = cfg.T, args.steps
     fw = r["forwards_per_step"]
     ms_step = r["ms_total"] / K
-    tokens_s = fw * T * world * K / (r["ms_total"] / 1e3)
+    tokens_s = weak_scaling_value(fw * T, K, world, r["ms_total"])
     flops = cfg.flops()
     st = r["stage_ms"]
     gu_bytes = gate_up_bytes(cfg, r["counts"], T)
