@@ -36,7 +36,7 @@ it) and is rounded to BF16 once, after the float64 sum shared + sum_k g_k * Y_k.
 import numpy as np
 
 from .formats import e4m3_decode, bf16_round
-from .quant import quant_1x128
+from .quant import quant_1x128, quant_1x128_pow2
 
 
 def blockscaled_gemm(qa, sa, qb, sb):
@@ -59,12 +59,13 @@ def blockscaled_gemm(qa, sa, qb, sb):
     return C
 
 
-def swiglu_expert(xq, sx, w1q, s1, w3q, s3, w2q, s2):
+def swiglu_expert(xq, sx, w1q, s1, w3q, s3, w2q, s2, pow2=False):
     """One SwiGLU expert on FP8 rows.
 
     xq uint8 [m, d] with sx float32 [d/128, m]; w1q/w3q uint8 [f, d] (gate / up) with
     s1/s3 float32 [f/128, d/128]; w2q uint8 [d, f] with s2 float32 [d/128, f/128].
     Returns (hq uint8 [m, f], sh float32 [f/128, m], Y float32 [m, d] of BF16 values).
+    pow2: h is requantised with power-of-two scales (the MX-native variant).
     """
     g = blockscaled_gemm(xq, sx, w1q, s1).astype(np.float32)
     u = blockscaled_gemm(xq, sx, w3q, s3).astype(np.float32)
@@ -72,7 +73,7 @@ def swiglu_expert(xq, sx, w1q, s1, w3q, s3, w2q, s2):
     with np.errstate(over="ignore"):
         silu = gd / (1.0 + np.exp(-gd))
     h = (silu * u.astype(np.float64)).astype(np.float32)
-    hq, sh = quant_1x128(h)
+    hq, sh = quant_1x128_pow2(h) if pow2 else quant_1x128(h)
     y = bf16_round(blockscaled_gemm(hq, sh, w2q, s2))
     return hq, sh, y
 
