@@ -55,6 +55,11 @@ def parse():
                                          "sweep_mx"],
                     default="v3")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--mx", action="store_true",
+                    help="layer configs: the MX-native variant (power-of-two scales applied by "
+                         "the tensor core) instead of FP32 scales with software promotion")
+    ap.add_argument("--shape", default=None,
+                    help="sweep configs only: one M,N,K instead of the five sweep shapes")
     return ap.parse_args()
 
 
@@ -244,10 +249,10 @@ def run_layer(args, cfg, rank, world, dev):
     from fp8_block_scaled_bias_b300.layer import MoELayer as _L
 
     T = cfg.T
-    w = make_weights(cfg, dev)
+    w = make_weights(cfg, dev, pow2=args.mx)
     x_host = workloads.gen_x(cfg, base_seed=rank).pin_memory()
     x = x_host.to(dev)
-    layer = MoELayer(cfg, w)
+    layer = MoELayer(cfg, w, mx=args.mx)
     skewed = cfg.zipf_s > 0
     bias0 = w.bias.clone()
     stages = list(_L.STAGE_LAUNCHES) + (["bias_update"] if skewed else [])
@@ -437,9 +442,10 @@ def main_ours(args, cfg, rank, world, dev):
     # the kernel runs inside a seconds-long step: the sustained peak applies
     fp8_peak = 2.0 * pk["bf16_tflops_sustained"]
     gemm_ms = (st["gate_up"] + st["down"]) / fw
-    roof = kernel_roofline("fp8_gemm_kernel<SwiGLU> (gate/up grouped GEMM)", gu_bytes,
+    roof = kernel_roofline("fp8_mx_gemm_kernel<SwiGLU> (gate/up grouped GEMM)" if args.mx else
+                           "fp8_gemm_kernel<SwiGLU> (gate/up grouped GEMM)", gu_bytes,
                            gate_up_flops(cfg, T), gu_ms, pk, fp8_peak)
-    roof["traffic"] = committed_traffic() if cfg.name == "v3" else None
+    roof["traffic"] = committed_traffic() if cfg.name == "v3" and not args.mx else None
     roof["peak_source"] = pk["source"] + (" (fp8 = 2 x sustained bf16, the nominal ratio)"
                                           if roof["bound"] == "tensor" else " (copy)")
     layer_bytes = gu_bytes + down_bytes(cfg, r["counts"], T)
@@ -449,6 +455,9 @@ def main_ours(args, cfg, rank, world, dev):
     if fw == 2:
         workload += (f"; Zipf({cfg.zipf_s}) bias; each step: forward, bias update "
                      f"gamma={GAMMA}, forward (2T tokens)")
+    if args.mx:
+        workload += ("; MX-native variant: power-of-two block scales applied by the tensor "
+                     "core (tcgen05 kind::mxf8f6f4)")
     out = {
         "metric": METRIC, "value": round(tokens_s, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
@@ -524,7 +533,10 @@ def main_sweep(args, rank, dev, mx=False):
     from fp8_block_scaled_bias_b300 import ops
     pk = peaks()
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
-    for (M, N, K) in workloads.GEMM_SWEEP:
+    shapes = workloads.GEMM_SWEEP
+    if args.shape:
+        shapes = [tuple(int(v) for v in args.shape.split(","))]
+    for (M, N, K) in shapes:
         a = workloads.gen_normal(M, K, sub_seed=31, device="cuda").to(torch.bfloat16)
         b = workloads.gen_normal(N, K, sub_seed=32, device="cuda")
         qa, sa = ops.quant_1x128(a, pow2=mx)

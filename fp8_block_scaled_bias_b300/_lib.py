@@ -33,6 +33,8 @@ SIGNATURES = {
     "fp8_quant_1x128_pow2": (_I, [_P, _I, _I, _I, _P, _P, _P]),
     "fp8_quant_128x128_pow2": (_I, [_P, _I, _I, _P, _P, _P]),
     "fp8_mx_grouped_gemm": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _I, _P, _P]),
+    "fp8_quant_scatter_1x128_pow2": (_I, [_P, _I, _I, _I, _P, _I, _I, _I, _P, _P, _P, _P]),
+    "moe_gate_up_mx": (_I, [_P, _P, _P, _I, _P, _P, _I, _I, _I, _P, _P, _P, _P]),
     "fp8_blockscaled_grouped_gemm": (_I, [_P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P, _I,
                                           _P, _P, _SZ, _P]),
     "fp8_grouped_gemm_ws_bytes": (_SZ, [_I, _I, _I]),

@@ -139,9 +139,10 @@ int fp8_quant_1x128_pow2(const uint16_t* x, int rows, int cols, int ldx, uint8_t
   return quant_1x128_common(x, rows, cols, ldx, q, scale, true, stream);
 }
 
-int fp8_quant_scatter_1x128(const uint16_t* x, int T, int cols, int ldx, const int32_t* row_of,
-                            int K, int shared_row_base, int n_rows, uint8_t* q, float* scale,
-                            int32_t* dev_status, void* stream) {
+static int quant_scatter_common(const uint16_t* x, int T, int cols, int ldx,
+                                const int32_t* row_of, int K, int shared_row_base, int n_rows,
+                                uint8_t* q, float* scale, bool pow2, int32_t* dev_status,
+                                void* stream) {
   if (T < 0 || K < 0 || n_rows < 0 || cols < 0 || cols % 128 != 0 || ldx < cols || ldx % 8 != 0)
     return MOE_ERR_INVALID_ARG;
   if (T == 0 || cols == 0) return MOE_OK;
@@ -149,7 +150,21 @@ int fp8_quant_scatter_1x128(const uint16_t* x, int T, int cols, int ldx, const i
       (reinterpret_cast<uintptr_t>(q) & 7u))
     return MOE_ERR_INVALID_ARG;
   return moe::launch_quant_scatter_1x128(x, T, cols, ldx, row_of, K, shared_row_base, n_rows, q,
-                                         scale, dev_status, as_stream(stream));
+                                         scale, pow2, dev_status, as_stream(stream));
+}
+
+int fp8_quant_scatter_1x128(const uint16_t* x, int T, int cols, int ldx, const int32_t* row_of,
+                            int K, int shared_row_base, int n_rows, uint8_t* q, float* scale,
+                            int32_t* dev_status, void* stream) {
+  return quant_scatter_common(x, T, cols, ldx, row_of, K, shared_row_base, n_rows, q, scale,
+                              false, dev_status, stream);
+}
+
+int fp8_quant_scatter_1x128_pow2(const uint16_t* x, int T, int cols, int ldx,
+                                 const int32_t* row_of, int K, int shared_row_base, int n_rows,
+                                 uint8_t* q, float* scale, int32_t* dev_status, void* stream) {
+  return quant_scatter_common(x, T, cols, ldx, row_of, K, shared_row_base, n_rows, q, scale,
+                              true, dev_status, stream);
 }
 
 static int quant_128x128_common(const float* w, int rows, int cols, uint8_t* q, float* scale,
@@ -195,8 +210,8 @@ int fp8_mx_grouped_gemm(const uint8_t* A, const float* sA, const uint8_t* B, con
   if (!A || !sA || !B || !sB || !seg_offsets || !C) return MOE_ERR_INVALID_ARG;
   if (ldc < N || ldc % 8 != 0 || !aligned16(A) || !aligned16(B) || !aligned16(C))
     return MOE_ERR_INVALID_ARG;
-  return moe::launch_mx_gemm(A, sA, B, sB, seg_offsets, G, M, N, K, C, ldc, dev_status,
-                             as_stream(stream));
+  return moe::launch_mx_gemm(A, sA, B, sB, seg_offsets, G, M, N, K, C, ldc, nullptr, nullptr,
+                             moe::kEpiBF16, dev_status, as_stream(stream));
 }
 
 int fp8_blockscaled_grouped_gemm(const uint8_t* A, const float* sA, int M_a,
@@ -306,6 +321,20 @@ int moe_gate_up_fp8(const uint8_t* xq_rows, const float* sx_rows, const int32_t*
   up.G = n_segments; up.M = rows; up.N = 2 * f; up.K = d;
   up.hq = hq; up.sh = sh; up.status = dev_status;
   return moe::launch_fp8_gemm(up, moe::kEpiSwiGLU, as_stream(stream));
+}
+
+int moe_gate_up_mx(const uint8_t* xq_rows, const float* sx_rows, const int32_t* offsets,
+                   int rows, const uint8_t* w13, const float* s13, int n_segments, int d, int f,
+                   uint8_t* hq, float* sh, int32_t* dev_status, void* stream) {
+  if (rows < 0 || d <= 0 || f <= 0 || d % 128 != 0 || f % 128 != 0 || n_segments < 1)
+    return MOE_ERR_INVALID_ARG;
+  const int st = check_gemm_dims(n_segments, rows, 2 * f, d);
+  if (st != MOE_OK) return st;
+  if (rows == 0) return MOE_OK;
+  if (!xq_rows || !sx_rows || !offsets || !w13 || !s13 || !hq || !sh) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(xq_rows) || !aligned16(w13) || !aligned16(hq)) return MOE_ERR_INVALID_ARG;
+  return moe::launch_mx_gemm(xq_rows, sx_rows, w13, s13, offsets, n_segments, rows, 2 * f, d,
+                             nullptr, 0, hq, sh, moe::kEpiSwiGLU, dev_status, as_stream(stream));
 }
 
 // ---- combine, bias update, workspace -------------------------------------------------

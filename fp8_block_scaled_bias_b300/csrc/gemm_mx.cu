@@ -58,7 +58,9 @@ constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;   // tmem slot, abort, total, b
 constexpr int OFF_SEG = OFF_MISC + 16;
 constexpr int OFF_USTART = OFF_SEG + (MAX_G + 1) * 4;
 constexpr int OFF_WSUM = OFF_USTART + (MAX_G + 1) * 4;
-constexpr int SMEM_USED = OFF_WSUM + 32 * 4;
+constexpr int OFF_AMAX = OFF_WSUM + 32 * 4;       // [2 tiles][2 column halves][128 rows]
+constexpr int SMEM_USED = OFF_AMAX + 2 * 2 * BM * 4;
+constexpr int EPI_BAR = 2;                          // named barrier of the 8 epilogue warps
 constexpr int SMEM_ALLOC = SMEM_USED + 1024;
 static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 
@@ -79,6 +81,8 @@ struct MxParams {
   int G, M, N, K;
   uint16_t* C;
   int ldc;
+  uint8_t* hq;           // SwiGLU epilogue: [M][N/2] E4M3
+  float* sh;             // SwiGLU epilogue: [N/256][M] power-of-two scales
   int32_t* status;
 };
 
@@ -120,6 +124,22 @@ MOE_DEV uint32_t ue8m0_word(float s, bool& bad) {
   return e * 0x01010101u;
 }
 
+MOE_DEV float silu_mx(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
+
+// The power-of-two scale rule of this variant: the smallest 2^k >= 2^-126 with
+// 448 * 2^k >= amax (448 = 1.75 * 2^8), exactly, from amax's exponent and mantissa.
+MOE_DEV float pow2_scale(float amax) {
+  if (amax == 0.0f) return 1.0f;
+  uint32_t b = __float_as_uint(amax);
+  int e = static_cast<int>((b >> 23) & 0xFFu) - 127;
+  if (((b >> 23) & 0xFFu) == 0) {
+    b = __float_as_uint(amax * 18446744073709551616.0f);   // * 2^64, exact
+    e = static_cast<int>((b >> 23) & 0xFFu) - 127 - 64;
+  }
+  const int k = max(e - 8 + ((b & 0x7FFFFFu) > 0x600000u ? 1 : 0), -126);
+  return __uint_as_float(static_cast<uint32_t>(k + 127) << 23);
+}
+
 MOE_DEV void decode_unit(int unit, const int* ustart, const int* seg, int G, int& g, int& m0,
                          int& rows_valid, int& nt) {
   int lo = 0, hi = G - 1;
@@ -146,6 +166,7 @@ MOE_DEV void mbar_drain_mx(uint32_t bar, uint32_t parity) {
 
 }  // namespace
 
+template <int EPI>
 __global__ void __launch_bounds__(mx::THREADS, 1)
     fp8_mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB, const MxParams p) {
@@ -169,6 +190,7 @@ __global__ void __launch_bounds__(mx::THREADS, 1)
   int* seg = reinterpret_cast<int*>(smem + OFF_SEG);
   int* ustart = reinterpret_cast<int*>(smem + OFF_USTART);
   int* wsum = reinterpret_cast<int*>(smem + OFF_WSUM);
+  float* amax_x = reinterpret_cast<float*>(smem + OFF_AMAX);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = p.G;
@@ -336,8 +358,13 @@ __global__ void __launch_bounds__(mx::THREADS, 1)
         }
         const uint32_t b0 = ue8m0_word(__ldg(sbg + static_cast<long long>(nb0) * KB + kb), badscale);
         const uint32_t b1 = ue8m0_word(__ldg(sbg + static_cast<long long>(nb1) * KB + kb), badscale);
+        // B row n of the tile is row 32 c + lane of column c.  Plain layout: rows [0, 128)
+        // belong to weight block 2 nt, [128, 256) to 2 nt + 1.  SwiGLU (gate/up interleaved
+        // in 64-row blocks): rows [0, 64) and [128, 192) are gate rows (block 2 nt of the
+        // scales, which alternate gate block, up block), [64, 128) and [192, 256) up rows.
 #pragma unroll
-        for (int c = 0; c < 8; ++c) wb[c] = c < 4 ? b0 : b1;
+        for (int c = 0; c < 8; ++c)
+          wb[c] = (EPI == kEpiSwiGLU ? ((c >> 1) & 1) : (c >> 2)) ? b1 : b0;
         const uint32_t col = tmem_base + lane_addr + SF_COL0 + j * SF_SLOT_COLS;
         tmem_st_x4(col, wa);
         tmem_st_x8(col + SFB_OFF, wb);
@@ -349,7 +376,7 @@ __global__ void __launch_bounds__(mx::THREADS, 1)
     }
     if (__any_sync(0xFFFFFFFFu, badscale) && lane == 0) set_status(p.status, MOE_ERR_DEVICE_DATA);
   } else if (warp >= EPI_WARP0 && warp < EPI_WARP0 + EPI_WARPS) {
-    // ---------------- epilogue: accumulator -> BF16 ----------------
+    // ---------------- epilogue ----------------
     const int q = warp & 3;
     const int grp = (warp - EPI_WARP0) >> 2;
     const int row = q * 32 + lane;
@@ -358,31 +385,83 @@ __global__ void __launch_bounds__(mx::THREADS, 1)
     for (int unit = first_unit; unit < total; unit += unit_stride, ++tt) {
       int g, m0, rv, nt;
       decode_unit(unit, ustart, seg, G, g, m0, rv, nt);
-      if (!mbar_wait_warp(tfull_bar, tt & 1, abort_flag, p.status)) break;
+      const bool good = mbar_wait_warp(tfull_bar, tt & 1, abort_flag, p.status);
+      // all eight warps agree before any of them uses the barrier below
+      if (named_bar_sync_or(EPI_BAR, EPI_WARPS * 32, !good)) break;
       tc_fence_after();
-      const int col0 = nt * BN + grp * 128;
-      const bool store = row < rv && col0 < p.N;
-      uint4* dst = reinterpret_cast<uint4*>(p.C + static_cast<long long>(m0 + row) * p.ldc + col0);
+      const uint32_t tbase = tmem_base + lane_addr + static_cast<uint32_t>(grp * 128);
+      if (EPI == kEpiBF16) {
+        const int col0 = nt * BN + grp * 128;
+        const bool store = row < rv && col0 < p.N;
+        uint4* dst =
+            reinterpret_cast<uint4*>(p.C + static_cast<long long>(m0 + row) * p.ldc + col0);
 #pragma unroll
-      for (int c = 0; c < 8; c += 2) {
-        uint32_t v[2][16];
-        const uint32_t ta = tmem_base + lane_addr + static_cast<uint32_t>(grp * 128 + c * 16);
-        tmem_ld_32x32b_x16(ta, v[0]);
-        tmem_ld_32x32b_x16(ta + 16, v[1]);
-        tmem_ld_wait();
-        if (store) {
+        for (int c = 0; c < 8; c += 2) {
+          uint32_t v[2][16];
+          tmem_ld_32x32b_x16(tbase + c * 16, v[0]);
+          tmem_ld_32x32b_x16(tbase + c * 16 + 16, v[1]);
+          tmem_ld_wait();
+          if (store) {
 #pragma unroll
-          for (int h = 0; h < 2; ++h)
+            for (int h = 0; h < 2; ++h)
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
-              uint4 o;
-              o.x = pack_bf16x2(__uint_as_float(v[h][8 * i + 0]), __uint_as_float(v[h][8 * i + 1]));
-              o.y = pack_bf16x2(__uint_as_float(v[h][8 * i + 2]), __uint_as_float(v[h][8 * i + 3]));
-              o.z = pack_bf16x2(__uint_as_float(v[h][8 * i + 4]), __uint_as_float(v[h][8 * i + 5]));
-              o.w = pack_bf16x2(__uint_as_float(v[h][8 * i + 6]), __uint_as_float(v[h][8 * i + 7]));
-              dst[(c + h) * 2 + i] = o;
-            }
+              for (int i = 0; i < 2; ++i) {
+                uint4 o;
+                o.x = pack_bf16x2(__uint_as_float(v[h][8 * i + 0]), __uint_as_float(v[h][8 * i + 1]));
+                o.y = pack_bf16x2(__uint_as_float(v[h][8 * i + 2]), __uint_as_float(v[h][8 * i + 3]));
+                o.z = pack_bf16x2(__uint_as_float(v[h][8 * i + 4]), __uint_as_float(v[h][8 * i + 5]));
+                o.w = pack_bf16x2(__uint_as_float(v[h][8 * i + 6]), __uint_as_float(v[h][8 * i + 7]));
+                dst[(c + h) * 2 + i] = o;
+              }
+          }
         }
+      } else {
+        // SwiGLU: columns [0, 64) of this half are gate rows, [64, 128) the matching up
+        // rows (64-row interleave of w13).  Pass 1 finds the row's max |h| over its 128
+        // hidden columns (64 here, 64 in the partner warp of the other half); pass 2
+        // reloads the accumulator, recomputes the same h and writes E4M3 codes.
+        float amax = 0.0f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[2][16];
+          tmem_ld_32x32b_x16(tbase + c * 16, v[0]);
+          tmem_ld_32x32b_x16(tbase + 64 + c * 16, v[1]);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            amax = fmaxf(amax, fabsf(__fmul_rn(silu_mx(__uint_as_float(v[0][i])),
+                                               __uint_as_float(v[1][i]))));
+        }
+        float* ax = amax_x + (tt & 1) * 2 * BM;
+        ax[grp * BM + row] = amax;
+        named_bar_sync_or(EPI_BAR, EPI_WARPS * 32, false);
+        amax = fmaxf(amax, ax[(grp ^ 1) * BM + row]);
+        const float sc = pow2_scale(amax);
+        const float rs = __frcp_rn(sc);                     // exact: sc is a power of two
+        const bool store = row < rv;
+        const int f = p.N / 2;
+        uint4* dst = reinterpret_cast<uint4*>(p.hq + static_cast<long long>(m0 + row) * f +
+                                              nt * 128 + grp * 64);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[2][16];
+          tmem_ld_32x32b_x16(tbase + c * 16, v[0]);
+          tmem_ld_32x32b_x16(tbase + 64 + c * 16, v[1]);
+          tmem_ld_wait();
+          uint32_t w[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            float h[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              h[i] = __fmul_rn(__fmul_rn(silu_mx(__uint_as_float(v[0][4 * j + i])),
+                                         __uint_as_float(v[1][4 * j + i])),
+                               rs);
+            w[j] = f32x2_to_e4m3x2(h[0], h[1]) | (f32x2_to_e4m3x2(h[2], h[3]) << 16);
+          }
+          if (store) dst[c] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        if (store && grp == 0) p.sh[static_cast<long long>(nt) * p.M + m0 + row] = sc;
       }
       tc_fence_before();
       __syncwarp();
@@ -404,11 +483,30 @@ bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* ptr
                     uint64_t inner, uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
                     uint32_t box_outer);   // runtime.cu
 
+namespace {
+template <int EPI>
+int launch_mx_kernel(const CUtensorMap& tmA, const CUtensorMap& tmB, const MxParams& p,
+                     long long grid, cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(fp8_mx_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             mx::SMEM_ALLOC) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    attr_set = true;
+  }
+  fp8_mx_gemm_kernel<EPI><<<static_cast<unsigned>(grid), mx::THREADS, mx::SMEM_ALLOC, stream>>>(
+      tmA, tmB, p);
+  return check_launch();
+}
+}  // namespace
+
 int launch_mx_gemm(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
                    const int32_t* seg, int G, int M, int N, int K, uint16_t* C, int ldc,
-                   int32_t* status, cudaStream_t stream) {
+                   uint8_t* hq, float* sh, GemmEpilogue epi, int32_t* status,
+                   cudaStream_t stream) {
   using namespace mx;
   if (M == 0) return MOE_OK;
+  if (N % 128 != 0 || (epi == kEpiSwiGLU && N % BN != 0)) return MOE_ERR_UNSUPPORTED;
   CUtensorMap tmA, tmB;
   if (!encode_tmap_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, K, BK, BM)) return MOE_ERR_CUDA;
   if (!encode_tmap_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, static_cast<uint64_t>(G) * N, K,
@@ -417,20 +515,13 @@ int launch_mx_gemm(const uint8_t* A, const float* sA, const uint8_t* B, const fl
   MxParams p;
   p.sA = sA; p.sB = sB; p.seg = seg;
   p.G = G; p.M = M; p.N = N; p.K = K;
-  p.C = C; p.ldc = ldc; p.status = status;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(fp8_mx_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             SMEM_ALLOC) != cudaSuccess)
-      return MOE_ERR_CUDA;
-    attr_set = true;
-  }
+  p.C = C; p.ldc = ldc; p.hq = hq; p.sh = sh; p.status = status;
   const long long units = (static_cast<long long>(M) / BM + G) * ((N + BN - 1) / BN);
   long long grid = num_sms();
   if (units < grid) grid = units;
   if (grid < 1) grid = 1;
-  fp8_mx_gemm_kernel<<<static_cast<unsigned>(grid), THREADS, SMEM_ALLOC, stream>>>(tmA, tmB, p);
-  return check_launch();
+  if (epi == kEpiSwiGLU) return launch_mx_kernel<kEpiSwiGLU>(tmA, tmB, p, grid, stream);
+  return launch_mx_kernel<kEpiBF16>(tmA, tmB, p, grid, stream);
 }
 
 }  // namespace moe

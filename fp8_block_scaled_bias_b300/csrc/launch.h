@@ -22,15 +22,11 @@ int launch_quant_1x128(const uint16_t* x, int rows, int cols, int ldx, uint8_t* 
 // row_of[t][0..K-1] and, if shared_row_base >= 0, shared_row_base + t of q / scale.
 int launch_quant_scatter_1x128(const uint16_t* x, int T, int cols, int ldx, const int32_t* row_of,
                                int K, int shared_row_base, int n_rows, uint8_t* q, float* scale,
-                               int32_t* status, cudaStream_t stream);
+                               bool pow2, int32_t* status, cudaStream_t stream);
 int launch_quant_128x128(const float* w, int rows, int cols, uint8_t* q, float* scale,
                          bool pow2, cudaStream_t stream);
 
-// MX-native grouped GEMM (gemm_mx.cu): power-of-two block scales applied by the tensor
-// core; BF16 output.  A rows already in segment order.
-int launch_mx_gemm(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
-                   const int32_t* seg, int G, int M, int N, int K, uint16_t* C, int ldc,
-                   int32_t* status, cudaStream_t stream);
+
 
 int launch_route(const float* scores, int aff, const float* bias, int T, int E, int n_groups,
                  int topk_groups, int group_topn, int K, float route_scale, int32_t* idx,
@@ -82,6 +78,14 @@ struct GemmArgs {
   int32_t* status;
 };
 int launch_fp8_gemm(const GemmArgs& a, GemmEpilogue epi, cudaStream_t stream);
+
+// MX-native grouped GEMM (gemm_mx.cu): power-of-two block scales applied by the tensor
+// core.  A rows already in segment order.  kEpiBF16 writes C; kEpiSwiGLU writes hq / sh
+// (power-of-two requantisation of h).
+int launch_mx_gemm(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
+                   const int32_t* seg, int G, int M, int N, int K, uint16_t* C, int ldc,
+                   uint8_t* hq, float* sh, GemmEpilogue epi, int32_t* status,
+                   cudaStream_t stream);
 
 int launch_router_logits(const uint16_t* x, int T, int d, const uint16_t* w_hilo, int E,
                          float* z, int32_t* status, void* ws, cudaStream_t stream);

@@ -90,6 +90,7 @@ __global__ void __launch_bounds__(256) quant_1x128_kernel(const uint16_t* __rest
 // BF16 combine").  Bit for bit the same as quant_1x128_kernel followed by a row gather
 // with the inverse map: the same per-tile arithmetic, written to more places.
 // One block per token (grid-stride); a half-warp per 1x128 tile.
+template <bool POW2>
 __global__ void __launch_bounds__(256) quant_scatter_1x128_kernel(
     const uint16_t* __restrict__ x, int T, int ldx, int ncb, const int32_t* __restrict__ row_of,
     int K, int shared_row_base, int n_rows, uint8_t* __restrict__ q, float* __restrict__ scale,
@@ -119,7 +120,7 @@ __global__ void __launch_bounds__(256) quant_scatter_1x128_kernel(
 #pragma unroll
       for (int off = 8; off > 0; off >>= 1)
         amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
-      const float s = e4m3_scale_from_amax(amax);
+      const float s = scale_rule<POW2>(amax);
       uint32_t out[2];
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
@@ -143,12 +144,16 @@ __global__ void __launch_bounds__(256) quant_scatter_1x128_kernel(
 
 int launch_quant_scatter_1x128(const uint16_t* x, int T, int cols, int ldx, const int32_t* row_of,
                                int K, int shared_row_base, int n_rows, uint8_t* q, float* scale,
-                               int32_t* status, cudaStream_t stream) {
+                               bool pow2, int32_t* status, cudaStream_t stream) {
   if (T == 0 || cols == 0) return MOE_OK;
   const int cap = num_sms() * 8;
   const int blocks = T < cap ? T : cap;
-  quant_scatter_1x128_kernel<<<blocks, 256, 0, stream>>>(x, T, ldx, cols / 128, row_of, K,
-                                                         shared_row_base, n_rows, q, scale, status);
+  if (pow2)
+    quant_scatter_1x128_kernel<true><<<blocks, 256, 0, stream>>>(
+        x, T, ldx, cols / 128, row_of, K, shared_row_base, n_rows, q, scale, status);
+  else
+    quant_scatter_1x128_kernel<false><<<blocks, 256, 0, stream>>>(
+        x, T, ldx, cols / 128, row_of, K, shared_row_base, n_rows, q, scale, status);
   return check_launch();
 }
 

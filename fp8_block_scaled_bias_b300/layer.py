@@ -11,6 +11,10 @@ the residual; ``forward(..., residual=True)`` adds x afterwards.
 Weights are prepared once (not timed): expert matrices are quantised 128x128 on the
 GPU and the gate/up matrices are interleaved in 64-row blocks so one 128-column GEMM
 tile holds matching gate and up columns.
+
+``mx=True`` runs the MX-native variant: power-of-two scales for x, the weights and h,
+applied by the tensor core (tcgen05 kind::mxf8f6f4) instead of by software promotion;
+its weights come from ``make_weights(..., pow2=True)``.
 """
 
 from dataclasses import dataclass
@@ -44,16 +48,17 @@ def interleave_gate_up(q1, s1, q3, s3):
     return w13.reshape(2 * f, d), s13.reshape(2 * f // 128, d // 128)
 
 
-def quantise_expert(w1, w3, w2):
-    """FP32 (w1 [f,d], w3 [f,d], w2 [d,f]) on the GPU -> (w13, s13, w2q, s2) via the library."""
-    q1, s1 = ops.quant_128x128(w1.contiguous())
-    q3, s3 = ops.quant_128x128(w3.contiguous())
-    q2, s2 = ops.quant_128x128(w2.contiguous())
+def quantise_expert(w1, w3, w2, pow2=False):
+    """FP32 (w1 [f,d], w3 [f,d], w2 [d,f]) on the GPU -> (w13, s13, w2q, s2) via the library
+    (pow2: power-of-two scales, for the MX-native variant)."""
+    q1, s1 = ops.quant_128x128(w1.contiguous(), pow2=pow2)
+    q3, s3 = ops.quant_128x128(w3.contiguous(), pow2=pow2)
+    q2, s2 = ops.quant_128x128(w2.contiguous(), pow2=pow2)
     w13, s13 = interleave_gate_up(q1, s1, q3, s3)
     return w13, s13, q2, s2
 
 
-def make_weights(cfg, device="cuda", base_seed=0, expert_fn=None):
+def make_weights(cfg, device="cuda", base_seed=0, expert_fn=None, pow2=False):
     """Seeded synthetic weights for ``cfg`` (a workloads.MoEConfig), quantised on the GPU.
 
     ``expert_fn(e)`` may override the FP32 expert generator (returns w1, w3, w2)."""
@@ -71,7 +76,7 @@ def make_weights(cfg, device="cuda", base_seed=0, expert_fn=None):
             w = workloads.gen_expert_f32(cfg, e, device=dev, base_seed=base_seed)
         else:
             w = tuple(t.to(dev) for t in expert_fn(e))
-        w13[e], s13[e], w2[e], s2[e] = quantise_expert(*w)
+        w13[e], s13[e], w2[e], s2[e] = quantise_expert(*w, pow2=pow2)
         del w
     return MoEWeights(cen, ops.router_split_bf16(cen), bias, w13, s13, w2, s2)
 
@@ -79,9 +84,10 @@ def make_weights(cfg, device="cuda", base_seed=0, expert_fn=None):
 class MoELayer:
     """Buffers and the sequence of library calls for one layer forward."""
 
-    def __init__(self, cfg, weights, T=None):
+    def __init__(self, cfg, weights, T=None, mx=False):
         self.cfg = cfg
         self.w = weights
+        self.mx = mx
         self.T = cfg.T if T is None else T
         T, E, K, d, f = self.T, cfg.E, cfg.K, cfg.d, cfg.f
         dev = weights.w13.device
@@ -127,13 +133,14 @@ class MoELayer:
         mark("permute")
         # 1x128 quantisation straight into segment order (one pass over x)
         ops.quant_scatter_1x128(x, self.row_of, self.rows, self.T * cfg.K, self.status,
-                                out=(self.xq_rows, self.sx_rows))
+                                out=(self.xq_rows, self.sx_rows), pow2=self.mx)
         mark("quant_dispatch")
         ops.gate_up(self.xq_rows, self.sx_rows, self.offsets, w.w13, w.s13, self.status,
-                    out=(self.hq, self.sh))
+                    out=(self.hq, self.sh), mx=self.mx)
         mark("gate_up")
-        ops.grouped_gemm(self.hq, self.sh, w.w2, w.s2, self.offsets, self.rows,
-                         status=self.status, out=self.y_rows)
+        down = ops.mx_grouped_gemm if self.mx else ops.grouped_gemm
+        down(self.hq, self.sh, w.w2, w.s2, self.offsets, self.rows, status=self.status,
+             out=self.y_rows)
         mark("down")
         ops.combine(self.y_rows, self.row_of, self.gate, self.T * cfg.K, self.status, out=self.y)
         mark("combine")

@@ -173,7 +173,8 @@ def quant_1x128(x, out=None, pow2=False):
     return q, s
 
 
-def quant_scatter_1x128(x, row_of, n_rows, shared_row_base=None, status=None, out=None):
+def quant_scatter_1x128(x, row_of, n_rows, shared_row_base=None, status=None, out=None,
+                        pow2=False):
     """Quantise each token row of x once and write it to rows row_of[t, :] and (if
     shared_row_base is not None) shared_row_base + t: bit for bit quant_1x128 followed by
     gather_rows with the inverse map."""
@@ -187,8 +188,8 @@ def quant_scatter_1x128(x, row_of, n_rows, shared_row_base=None, status=None, ou
     else:
         q, s = out
     base = -1 if shared_row_base is None else int(shared_row_base)
-    call("fp8_quant_scatter_1x128", _ptr(x), T, cols, cols, _ptr(row_of), K, base, n_rows,
-         _ptr(q), _ptr(s), _ptr(status), _stream())
+    call("fp8_quant_scatter_1x128_pow2" if pow2 else "fp8_quant_scatter_1x128", _ptr(x), T,
+         cols, cols, _ptr(row_of), K, base, n_rows, _ptr(q), _ptr(s), _ptr(status), _stream())
     return q, s
 
 
@@ -284,8 +285,9 @@ def gather_rows(src, src_scale, rows, row_limit=None, status=None, out=None):
     return dst, dsc
 
 
-def gate_up(xq_rows, sx_rows, offsets, w13, s13, status=None, out=None):
-    """hq, sh = requantised silu(gate) * up over expert segments (rows in segment order)."""
+def gate_up(xq_rows, sx_rows, offsets, w13, s13, status=None, out=None, mx=False):
+    """hq, sh = requantised silu(gate) * up over expert segments (rows in segment order);
+    mx: the MX-native variant (power-of-two scales in and out)."""
     for t, dt, n in ((xq_rows, _U8, "xq_rows"), (sx_rows, _F32, "sx_rows"),
                      (offsets, _I32, "offsets"), (w13, _U8, "w13"), (s13, _F32, "s13")):
         _check(t, dt, n)
@@ -297,8 +299,9 @@ def gate_up(xq_rows, sx_rows, offsets, w13, s13, status=None, out=None):
         sh = torch.empty(f // 128, rows, dtype=_F32, device=xq_rows.device)
     else:
         hq, sh = out
-    call("moe_gate_up_fp8", _ptr(xq_rows), _ptr(sx_rows), _ptr(offsets), rows, _ptr(w13),
-         _ptr(s13), S, d, f, _ptr(hq), _ptr(sh), _ptr(status), _stream())
+    call("moe_gate_up_mx" if mx else "moe_gate_up_fp8", _ptr(xq_rows), _ptr(sx_rows),
+         _ptr(offsets), rows, _ptr(w13), _ptr(s13), S, d, f, _ptr(hq), _ptr(sh), _ptr(status),
+         _stream())
     return hq, sh
 
 

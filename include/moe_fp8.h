@@ -181,11 +181,15 @@ int fp8_quant_128x128(const float* w, int rows, int cols, uint8_t* q, float* sca
  * 448 * s >= amax (at least 2^-126; s = 1 when amax == 0), so x / s is exact and never
  * saturates.  The pages note that the 1x128 / 128x128 groups match the microscaling
  * formats Blackwell tensor cores take natively ([sum] core idea 6(a)) and mention
- * power-of-two scales ([book] ch. 17 "Attention-related saved activations"). */
+ * power-of-two scales ([book] ch. 17 "Attention-related saved activations").  The
+ * scatter form is fp8_quant_scatter_1x128 with this rule. */
 int fp8_quant_1x128_pow2(const uint16_t* x, int rows, int cols, int ldx, uint8_t* q,
                          float* scale, void* stream);
 int fp8_quant_128x128_pow2(const float* w, int rows, int cols, uint8_t* q, float* scale,
                            void* stream);
+int fp8_quant_scatter_1x128_pow2(const uint16_t* x, int T, int cols, int ldx,
+                                 const int32_t* row_of, int K, int shared_row_base, int n_rows,
+                                 uint8_t* q, float* scale, int32_t* dev_status, void* stream);
 
 /* ---- FP8 block-scaled grouped GEMM ------------------------------------------------- */
 
@@ -219,6 +223,14 @@ size_t fp8_grouped_gemm_ws_bytes(int M, int K, int has_a_rows);
 int fp8_mx_grouped_gemm(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
                         const int32_t* seg_offsets, int G, int M, int N, int K, uint16_t* C,
                         int ldc, int32_t* dev_status, void* stream);
+
+/* MX-native gate/up: moe_gate_up_fp8 on power-of-two scales (x rows, w13), with h
+ * requantised 1x128 by the power-of-two rule of fp8_quant_1x128_pow2, so hq / sh feed
+ * fp8_mx_grouped_gemm for the down projection.  Same layouts and limits as
+ * moe_gate_up_fp8; a scale that is not a power of two sets MOE_ERR_DEVICE_DATA. */
+int moe_gate_up_mx(const uint8_t* xq_rows, const float* sx_rows, const int32_t* offsets,
+                   int rows, const uint8_t* w13, const float* s13, int n_segments, int d, int f,
+                   uint8_t* hq, float* sh, int32_t* dev_status, void* stream);
 
 /* ---- experts ----------------------------------------------------------------------- */
 

@@ -20,11 +20,12 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-def _oracle_experts(cfg):
+def _oracle_experts(cfg, pow2=False):
+    qw = oracle.quant_128x128_pow2 if pow2 else oracle.quant_128x128
     ex = []
     for e in range(cfg.E + 1):
         w = [t.cpu().numpy() for t in workloads.gen_expert_f32(cfg, e, device="cuda")]
-        ex.append(tuple(a for m in w for a in oracle.quant_128x128(m)))
+        ex.append(tuple(a for m in w for a in qw(m)))
     return ex
 
 
@@ -184,23 +185,25 @@ def _pool():
     return _POOL
 
 
-def _sampled_outputs(cfg, layer, x, bias, tokens, i_ref):
+def _sampled_outputs(cfg, layer, x, bias, tokens, i_ref, pow2=False):
     """Oracle outputs of the sampled tokens; the experts they use are generated from the
     same seeds and quantised by the oracle (in parallel worker processes)."""
     need = sorted(set(int(e) for t in tokens for e in i_ref[t]) | {cfg.E})
     mats = []
     for e in need:
         mats.extend(t.cpu().numpy() for t in workloads.gen_expert_f32(cfg, e, device="cuda"))
-    quant = list(_pool().map(oracle.quant_128x128, mats))
+    qw = oracle.quant_128x128_pow2 if pow2 else oracle.quant_128x128
+    quant = list(_pool().map(qw, mats))
     q = {e: tuple(a for j in range(3) for a in quant[3 * i + j]) for i, e in enumerate(need)}
     return oracle.moe_layer_tokens(tokens, x.float().numpy()[tokens],
                                    layer.w.centroids.cpu().numpy(), bias, None, cfg.n_groups,
-                                   cfg.topk_groups, cfg.K, expert_quantised=q.__getitem__)
+                                   cfg.topk_groups, cfg.K, expert_quantised=q.__getitem__,
+                                   pow2=pow2)
 
 
-def _check_config(cfg, w, n_sample):
+def _check_config(cfg, w, n_sample, mx=False):
     x = workloads.gen_x(cfg)
-    layer = MoELayer(cfg, w)
+    layer = MoELayer(cfg, w, mx=mx)
     layer.forward(x.to(DEV))
     torch.cuda.synchronize()
     layer.check_status()
@@ -217,9 +220,9 @@ def _check_config(cfg, w, n_sample):
     rng = np.random.default_rng(cfg.T)
     cand = np.nonzero(same)[0]
     tokens = sorted(rng.choice(cand, n_sample, replace=False).tolist())
-    part = _sampled_outputs(cfg, layer, x, bias, tokens, i_ref)
+    part = _sampled_outputs(cfg, layer, x, bias, tokens, i_ref, pow2=mx)
     y = bf16_to_f32(layer.y)[tokens]
-    assert_close(y, part["y"], what=f"{cfg.name} sampled tokens")
+    assert_close(y, part["y"], what=f"{cfg.name} sampled tokens" + (" (MX)" if mx else ""))
     return layer
 
 
@@ -253,3 +256,42 @@ def test_skewed_layer_and_bias_update(v3_weights):
         assert c2[over].sum() <= counts[over].sum()      # overloaded experts lose load
     finally:
         w.bias.copy_(saved)
+
+
+# ---- the MX-native variant (power-of-two scales applied by the tensor core) -------------
+
+def test_tiny_mx_layer_from_identical_logits():
+    cfg = workloads.TINY
+    w = make_weights(cfg, DEV, pow2=True)
+    ex = _oracle_experts(cfg, pow2=True)
+    x = workloads.gen_x(cfg)
+    g = torch.Generator().manual_seed(5)
+    logits = (torch.randn(cfg.T, cfg.E, generator=g) * 1.5).float()
+    layer = MoELayer(cfg, w, mx=True)
+    layer.forward(x.to(DEV), logits=logits.to(DEV))
+    torch.cuda.synchronize()
+    layer.check_status()
+    ref = oracle.moe_layer(x.float().numpy(), w.centroids.cpu().numpy(), w.bias.cpu().numpy(),
+                           ex, cfg.n_groups, cfg.topk_groups, cfg.K, logits=logits.numpy(),
+                           pow2=True)
+    for name in ("idx", "counts", "offsets", "row_token", "row_of"):
+        assert np.array_equal(getattr(layer, name).cpu().numpy(), ref[name]), name
+    tok = ref["row_token"]
+    assert np.array_equal(layer.xq_rows.cpu().numpy(), ref["xq"][tok])
+    assert np.array_equal(layer.sx_rows.cpu().numpy(), ref["sx"][:, tok])
+    sh = layer.sh.cpu().numpy()
+    assert (np.frexp(sh.astype(np.float64))[0] == 0.5).all()        # powers of two
+    hq = oracle.dequant_1x128(layer.hq.cpu().numpy(), sh)
+    assert_close(hq, oracle.dequant_1x128(ref["hq"], ref["sh"]), max_rel=0.07, mae=5e-3,
+                 what="h (MX)")
+    assert_close(bf16_to_f32(layer.y_rows), ref["Y"], what="expert rows (MX)")
+    assert_close(bf16_to_f32(layer.y), ref["y"], what="layer output (MX)")
+
+
+def test_v3_mx_layer_sampled_tokens():
+    w = make_weights(workloads.V3, DEV, pow2=True)
+    try:
+        _check_config(workloads.V3, w, n_sample=3, mx=True)
+    finally:
+        del w
+        torch.cuda.empty_cache()

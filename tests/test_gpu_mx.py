@@ -143,3 +143,47 @@ def test_accuracy_against_the_fp32_scale_path(case):
         errs[pow2] = float((C - exact).abs().mean() / rms)
     assert errs[False] < 0.05 and errs[True] < 0.05, errs
     assert errs[True] <= 1.5 * errs[False], errs
+
+
+@pytest.mark.parametrize("mx", [False, True], ids=["fp32_scales", "mx"])
+def test_gate_up_with_distinct_gate_and_up_block_scales(mx):
+    """Gate and up weight blocks with different scales (the 64-row interleave must pair
+    every B row with its own block's scale) over ragged segments: h against the oracle's
+    SwiGLU of the exact block-scaled products."""
+    from fp8_block_scaled_bias_b300 import interleave_gate_up
+    seg = [0, 100, 100, 300]
+    S, d, f = len(seg) - 1, 512, 256
+    M = seg[-1]
+    rng = np.random.default_rng(17)
+    A = workloads.gen_fp8_codes(M, d, sub_seed=41)
+    sA = _pow2_scales((d // 128, M), 42, -3, 0)
+    w1 = [workloads.gen_fp8_codes(f, d, sub_seed=50 + e) for e in range(S)]
+    w3 = [workloads.gen_fp8_codes(f, d, sub_seed=60 + e) for e in range(S)]
+    s1 = [torch.from_numpy(np.exp2(rng.integers(-12, -9, (f // 128, d // 128))).astype(np.float32))
+          for _ in range(S)]
+    s3 = [torch.from_numpy(np.exp2(rng.integers(-6, -3, (f // 128, d // 128))).astype(np.float32))
+          for _ in range(S)]
+    if not mx:                                   # any positive scales for the FP32 path
+        s1 = [s * 1.37 for s in s1]
+    pairs = [interleave_gate_up(w1[e], s1[e], w3[e], s3[e]) for e in range(S)]
+    w13 = torch.stack([p[0] for p in pairs]).to(DEV)
+    s13 = torch.stack([p[1] for p in pairs]).to(DEV)
+    st = ops.new_status(DEV)
+    hq, sh = ops.gate_up(A.to(DEV), sA.to(DEV), torch.tensor(seg, dtype=torch.int32, device=DEV),
+                         w13, s13, st, mx=mx)
+    torch.cuda.synchronize()
+    assert ops.status_value(st) == 0
+    got = oracle.dequant_1x128(hq.cpu().numpy(), sh.cpu().numpy())
+    quant = oracle.quant_1x128_pow2 if mx else oracle.quant_1x128
+    ref = np.zeros((M, f))
+    for e in range(S):
+        r0, r1 = seg[e], seg[e + 1]
+        if r1 == r0:
+            continue
+        a, sa = A.numpy()[r0:r1], sA.numpy()[:, r0:r1]
+        g = oracle.blockscaled_gemm(a, sa, w1[e].numpy(), s1[e].numpy()).astype(np.float32)
+        u = oracle.blockscaled_gemm(a, sa, w3[e].numpy(), s3[e].numpy()).astype(np.float32)
+        gd = g.astype(np.float64)
+        h = (gd / (1 + np.exp(-gd)) * u).astype(np.float32)
+        ref[r0:r1] = oracle.dequant_1x128(*quant(h))
+    assert_close(got, ref, max_rel=0.07, mae=5e-3, what="h")
