@@ -145,9 +145,9 @@ static int quant_scatter_common(const uint16_t* x, int T, int cols, int ldx,
                                 void* stream) {
   if (T < 0 || K < 0 || n_rows < 0 || cols < 0 || cols % 128 != 0 || ldx < cols || ldx % 8 != 0)
     return MOE_ERR_INVALID_ARG;
+  if (K > 32) return MOE_ERR_UNSUPPORTED;
   if (T == 0 || cols == 0) return MOE_OK;
-  if (!x || (K > 0 && !row_of) || !q || !scale || !aligned16(x) ||
-      (reinterpret_cast<uintptr_t>(q) & 7u))
+  if (!x || (K > 0 && !row_of) || !q || !scale || !aligned16(x) || !aligned16(q))
     return MOE_ERR_INVALID_ARG;
   return moe::launch_quant_scatter_1x128(x, T, cols, ldx, row_of, K, shared_row_base, n_rows, q,
                                          scale, pow2, dev_status, as_stream(stream));

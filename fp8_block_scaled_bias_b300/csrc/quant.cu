@@ -89,54 +89,68 @@ __global__ void __launch_bounds__(256) quant_1x128_kernel(const uint16_t* __rest
 // pages quantise activations before dispatch, "DeepSeek-V3" book, ch. 17 "FP8 dispatch,
 // BF16 combine").  Bit for bit the same as quant_1x128_kernel followed by a row gather
 // with the inverse map: the same per-tile arithmetic, written to more places.
-// One block per token (grid-stride); a half-warp per 1x128 tile.
+// One block per token (grid-stride); eight lanes per 1x128 tile, 16 values each, so every
+// destination row gets 16-byte stores; the token's K destination rows are loaded once
+// (one per lane) and passed around with shuffles.
 template <bool POW2>
 __global__ void __launch_bounds__(256) quant_scatter_1x128_kernel(
     const uint16_t* __restrict__ x, int T, int ldx, int ncb, const int32_t* __restrict__ row_of,
     int K, int shared_row_base, int n_rows, uint8_t* __restrict__ q, float* __restrict__ scale,
     int32_t* status) {
-  const int hw = threadIdx.x >> 4;            // half-warp: 16 per block
-  const int hl = threadIdx.x & 15;
+  const int lane = threadIdx.x & 31;
+  const int slot = threadIdx.x >> 3;          // tile slot of this block iteration
+  const int el = threadIdx.x & 7;             // 16 values of the tile
+  const int slots = blockDim.x >> 3;
   const long long cols = static_cast<long long>(ncb) * 128;
-  const int ndst = K + (shared_row_base >= 0 ? 1 : 0);
   for (int t = blockIdx.x; t < T; t += gridDim.x) {
-    for (int cb0 = 0; cb0 < ncb; cb0 += 16) {  // uniform trip count: shuffles stay full-warp
-      const int cb = cb0 + hw;
+    const int my_row = lane < K ? row_of[static_cast<long long>(t) * K + lane] : 0;
+    for (int cb0 = 0; cb0 < ncb; cb0 += slots) {  // same trip count in every warp
+      const int cb = cb0 + slot;
       const bool valid = cb < ncb;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (valid)
-        v = __ldcs(reinterpret_cast<const uint4*>(x + static_cast<long long>(t) * ldx + cb * 128 +
-                                                  hl * 8));
-      float f[8];
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      uint4 v[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+      if (valid) {
+        const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<long long>(t) * ldx +
+                                                          cb * 128 + el * 16);
+        v[0] = __ldcs(src);
+        v[1] = __ldcs(src + 1);
+      }
+      float f[16];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        f[2 * i] = __uint_as_float(w[i] << 16);
-        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t w[4] = {v[h].x, v[h].y, v[h].z, v[h].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          f[8 * h + 2 * i] = __uint_as_float(w[i] << 16);
+          f[8 * h + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
       }
       float amax = 0.0f;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+      for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
 #pragma unroll
-      for (int off = 8; off > 0; off >>= 1)
+      for (int off = 4; off > 0; off >>= 1)
         amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
       const float s = scale_rule<POW2>(amax);
-      uint32_t out[2];
+      uint32_t out[4];
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
+      for (int i = 0; i < 4; ++i) {
         const uint32_t a = f32x2_to_e4m3x2(__fdiv_rn(f[4 * i], s), __fdiv_rn(f[4 * i + 1], s));
         const uint32_t b = f32x2_to_e4m3x2(__fdiv_rn(f[4 * i + 2], s), __fdiv_rn(f[4 * i + 3], s));
         out[i] = a | (b << 16);
       }
-      if (!valid) continue;
-      for (int k = 0; k < ndst; ++k) {
-        const int r = k < K ? row_of[static_cast<long long>(t) * K + k] : shared_row_base + t;
+      const uint4 o = make_uint4(out[0], out[1], out[2], out[3]);
+      for (int k = 0; k <= K; ++k) {
+        int r;
+        if (k < K) r = __shfl_sync(0xFFFFFFFFu, my_row, k);
+        else if (shared_row_base >= 0) r = shared_row_base + t;
+        else break;
+        if (!valid) continue;
         if (r < 0 || r >= n_rows) {
-          if (hl == 0 && cb == 0) set_status(status, MOE_ERR_DEVICE_DATA);
+          if (el == 0 && cb == 0) set_status(status, MOE_ERR_DEVICE_DATA);
           continue;
         }
-        *reinterpret_cast<uint2*>(q + r * cols + cb * 128 + hl * 8) = make_uint2(out[0], out[1]);
-        if (hl == 0) scale[static_cast<long long>(cb) * n_rows + r] = s;
+        *reinterpret_cast<uint4*>(q + r * cols + cb * 128 + el * 16) = o;
+        if (el == 0) scale[static_cast<long long>(cb) * n_rows + r] = s;
       }
     }
   }
@@ -146,14 +160,19 @@ int launch_quant_scatter_1x128(const uint16_t* x, int T, int cols, int ldx, cons
                                int K, int shared_row_base, int n_rows, uint8_t* q, float* scale,
                                bool pow2, int32_t* status, cudaStream_t stream) {
   if (T == 0 || cols == 0) return MOE_OK;
-  const int cap = num_sms() * 8;
+  // tile slots per block iteration: an even split of the row's tiles into <= 32 per pass
+  const int ncb = cols / 128;
+  const int passes = (ncb + 31) / 32;
+  const int slots = (ncb + passes - 1) / passes;
+  const int threads = (slots * 8 + 31) / 32 * 32;
+  const int cap = num_sms() * (2048 / threads);
   const int blocks = T < cap ? T : cap;
   if (pow2)
-    quant_scatter_1x128_kernel<true><<<blocks, 256, 0, stream>>>(
-        x, T, ldx, cols / 128, row_of, K, shared_row_base, n_rows, q, scale, status);
+    quant_scatter_1x128_kernel<true><<<blocks, threads, 0, stream>>>(
+        x, T, ldx, ncb, row_of, K, shared_row_base, n_rows, q, scale, status);
   else
-    quant_scatter_1x128_kernel<false><<<blocks, 256, 0, stream>>>(
-        x, T, ldx, cols / 128, row_of, K, shared_row_base, n_rows, q, scale, status);
+    quant_scatter_1x128_kernel<false><<<blocks, threads, 0, stream>>>(
+        x, T, ldx, ncb, row_of, K, shared_row_base, n_rows, q, scale, status);
   return check_launch();
 }
 

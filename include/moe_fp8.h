@@ -165,8 +165,8 @@ int fp8_quant_1x128(const uint16_t* x, int rows, int cols, int ldx, uint8_t* q,
  * row_token, in one pass over x: the pages quantise activations before dispatch ([book]
  * ch. 17 "FP8 dispatch, BF16 combine").  x: BF16 [T][cols] (pitch ldx); row_of: int32
  * [T][K]; q: uint8 [n_rows][cols]; scale: FP32 [cols/128][n_rows].  A destination
- * outside [0, n_rows) sets MOE_ERR_DEVICE_DATA and is skipped.  Alignment as for
- * fp8_quant_1x128. */
+ * outside [0, n_rows) sets MOE_ERR_DEVICE_DATA and is skipped.  K <= 32; x and q 16-byte
+ * aligned, ldx % 8 == 0. */
 int fp8_quant_scatter_1x128(const uint16_t* x, int T, int cols, int ldx, const int32_t* row_of,
                             int K, int shared_row_base, int n_rows, uint8_t* q, float* scale,
                             int32_t* dev_status, void* stream);
