@@ -164,6 +164,9 @@ class ClockSampler:
                     ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.SMI_FIELDS,
                      "--format=csv,noheader,nounits", "-lms", "20"],
                     stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                # wait for the sampler's first line (taken before the timed region, not
+                # kept) so that even a short timed region is sampled
+                self.proc.stdout.readline()
             except Exception:
                 self.proc = None
         return self
