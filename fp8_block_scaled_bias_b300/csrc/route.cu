@@ -62,7 +62,35 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(
 
   // group score: sum of the group_topn best selection scores, added best first
   float gscore = -INFINITY;
-  if (lane < n_groups) {
+  if (gs == 32 && group_topn <= 2) {
+    // one expert of every group per lane (expert 32 j + lane of group j): the two best of
+    // each group by a butterfly over the warp, every step keeping the best two of four
+    // by the same (score descending, index ascending) order
+    for (int j = 0; j < n_groups; ++j) {
+      float v1 = c_s[j * 32 + lane], v2 = -INFINITY;
+      int i1 = lane, i2 = -1;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float o1 = __shfl_xor_sync(0xFFFFFFFFu, v1, off);
+        const int p1 = __shfl_xor_sync(0xFFFFFFFFu, i1, off);
+        const float o2 = __shfl_xor_sync(0xFFFFFFFFu, v2, off);
+        const int p2 = __shfl_xor_sync(0xFFFFFFFFu, i2, off);
+        // merge two ranked pairs (v1,i1) >= (v2,i2) and (o1,p1) >= (o2,p2)
+        if (ranks_before(o1, p1, v1, i1)) {
+          const bool second = p2 >= 0 && ranks_before(o2, p2, v1, i1);
+          v2 = second ? o2 : v1;
+          i2 = second ? p2 : i1;
+          v1 = o1;
+          i1 = p1;
+        } else if (p1 >= 0 && (i2 < 0 || ranks_before(o1, p1, v2, i2))) {
+          v2 = o1;
+          i2 = p1;
+        }
+      }
+      const float g = group_topn == 1 ? v1 : __fadd_rn(v1, v2);
+      if (lane == j) gscore = g;
+    }
+  } else if (lane < n_groups) {
     const float* g = c_s + lane * gs;
     float pv = INFINITY;
     int pi = -1;
