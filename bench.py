@@ -339,13 +339,14 @@ def _oracle_token_times(payload):
     """Worker (spawned with one BLAS/OpenMP thread): time oracle.moe_layer_tokens on one
     token per step."""
     import oracle
-    cfg, tokens, xr, cen, bias, q, steps = payload
+    cfg, tokens, xr, cen, bias, q, steps, pow2 = payload
     times = []
     for s in range(steps):
         i = s % len(tokens)
         t0 = time.perf_counter()
         oracle.moe_layer_tokens([tokens[i]], xr[i:i + 1], cen, bias, None, cfg.n_groups,
-                                cfg.topk_groups, cfg.K, expert_quantised=q.__getitem__)
+                                cfg.topk_groups, cfg.K, expert_quantised=q.__getitem__,
+                                pow2=pow2)
         times.append(time.perf_counter() - t0)
     return times
 
@@ -377,7 +378,7 @@ def _spawn_pool(workers):
     return cf.ProcessPoolExecutor(max_workers=workers, mp_context=mp.get_context("spawn"))
 
 
-def cpu_baseline(cfg, cen, bias, x_host, n_tokens=4, steps=None):
+def cpu_baseline(cfg, cen, bias, x_host, n_tokens=4, steps=None, pow2=False):
     """The oracle, as it stands, on a bounded sample: n_tokens tokens of the workload, one
     at a time through oracle.moe_layer_tokens (routing in float64/float32, every expert
     block-scaled GEMM exact in float64), in one process with one thread.  Expert weights
@@ -397,13 +398,14 @@ def cpu_baseline(cfg, cen, bias, x_host, n_tokens=4, steps=None):
     workers = max(1, min(16, (os.cpu_count() or 2) - 1))
     with _WorkerThreads(1):
         with _spawn_pool(workers) as pool:
-            quant = list(pool.map(oracle.quant_128x128, mats))
+            quant = list(pool.map(oracle.quant_128x128_pow2 if pow2 else oracle.quant_128x128,
+                                  mats))
         q = {e: tuple(a for j in range(3) for a in quant[3 * i + j]) for i, e in enumerate(need)}
         del mats, quant
         steps = steps or n_tokens
         with _spawn_pool(1) as pool:
             times = pool.submit(_oracle_token_times,
-                                (cfg, tokens, xr, cen, bias, q, steps)).result()
+                                (cfg, tokens, xr, cen, bias, q, steps, pow2)).result()
     return dict(value=len(times) / sum(times), times=times, tokens=tokens, cores=1)
 
 
@@ -489,7 +491,7 @@ def main_ours(args, cfg, rank, world, dev):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cb = cpu_baseline(cfg, r["weights"].centroids.cpu().numpy(),
-                          r["weights"].bias.cpu().numpy(), r["x"])
+                          r["weights"].bias.cpu().numpy(), r["x"], pow2=args.mx)
         out["cpu_baseline"] = {"value": round(cb["value"], 4), "unit": "tokens/s", "cores": cb["cores"],
                                "kind": "oracle",
                                "sample": f"{len(cb['times'])} tokens of this workload, one at a time "
