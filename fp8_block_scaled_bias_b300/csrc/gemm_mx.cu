@@ -566,14 +566,9 @@ int launch_mx_kernel(const uint8_t* A, const uint8_t* B, const MxParams& p, cuda
   if (!encode_tmap_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, p.K,
                       static_cast<uint64_t>(p.G) * p.N, p.K, mx::BK, TL::BN))
     return MOE_ERR_CUDA;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(fp8_mx_gemm_kernel<EPI, PAIR>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             TL::SMEM_ALLOC) != cudaSuccess)
-      return MOE_ERR_CUDA;
-    attr_set = true;
-  }
+  if (set_max_dynamic_smem(reinterpret_cast<const void*>(fp8_mx_gemm_kernel<EPI, PAIR>),
+                           TL::SMEM_ALLOC) != MOE_OK)
+    return MOE_ERR_CUDA;
   const long long units =
       (static_cast<long long>(p.M) / TL::BM + p.G) * ((p.N + TL::BN - 1) / TL::BN);
   long long grid = num_sms();

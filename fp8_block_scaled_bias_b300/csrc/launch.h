@@ -12,6 +12,9 @@ namespace moe {
 // Multiprocessor count of the current device (cached per device).
 int num_sms();
 
+// Raise a kernel's dynamic shared-memory limit on the current device (once per device).
+int set_max_dynamic_smem(const void* func, int bytes);
+
 // MOE_OK if the last launch succeeded, else MOE_ERR_CUDA (and clears the error).
 int check_launch();
 

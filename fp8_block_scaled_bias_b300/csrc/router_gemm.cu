@@ -194,8 +194,8 @@ int launch_router_logits(const uint16_t* x, int T, int d, const uint16_t* w_hilo
                       BN))
     return MOE_ERR_CUDA;
   RouterParams p{z, T, d, E, BN, status};
-  if (cudaFuncSetAttribute(router_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           SMEM_ALLOC) != cudaSuccess)
+  if (set_max_dynamic_smem(reinterpret_cast<const void*>(router_logits_kernel), SMEM_ALLOC) !=
+      MOE_OK)
     return MOE_ERR_CUDA;
   dim3 grid(E / BN, (T + BM - 1) / BM);
   router_logits_kernel<<<grid, THREADS, SMEM_ALLOC, stream>>>(tmX, tmW, p);

@@ -4,6 +4,8 @@
 // a GPU driver.
 #include <cuda.h>
 #include <mutex>
+#include <set>
+#include <utility>
 
 #include "common.cuh"
 #include "launch.h"
@@ -21,6 +23,21 @@ int num_sms() {
     cached[dev] = n;
   }
   return cached[dev];
+}
+
+int set_max_dynamic_smem(const void* func, int bytes) {
+  // cudaFuncSetAttribute applies to the current device: remember (function, device) pairs
+  static std::mutex mu;
+  static std::set<std::pair<const void*, int>> done;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.count({func, dev})) return MOE_OK;
+  if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  done.insert({func, dev});
+  return MOE_OK;
 }
 
 int check_launch() {
