@@ -187,3 +187,24 @@ def test_pow2_reconstruction_error_bound_and_weight_blocks():
     full = np.repeat(np.repeat(s.astype(np.float64), 128, 0), 128, 1)
     # half an E4M3 ulp (3 fraction bits) relative, or half the subnormal unit 2^-9
     assert (np.abs(w_hat - w) <= 2.0 ** -4 * np.abs(w) + full * 2.0 ** -10).all()
+
+
+def test_dequant_1x128_layout_distinct_scales():
+    """Each element is its code's E4M3 value (decoded by torch's float8_e4m3fn cast, a
+    library routine) times the scale of its own (K block, row): s[c // 128][r], the
+    K-block-major activation-scale layout.  Checked element by element in plain Python,
+    with a different power-of-two-free scale for every (row, K block) so a transposed or
+    shifted scale index cannot pass."""
+    import torch
+    rows, cols = 3, 384
+    rng = np.random.default_rng(11)
+    finite = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8)
+    q = finite[rng.integers(0, finite.size, (rows, cols))]
+    s = np.array([[1.0 + r + 10.0 * kb + 0.125 for r in range(rows)] for kb in range(cols // 128)],
+                 np.float32)                                     # [cols/128][rows]
+    dec = torch.from_numpy(q).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = oracle.dequant_1x128(q, s)
+    assert got.shape == (rows, cols)
+    for r in range(rows):
+        for c in range(cols):
+            assert got[r, c] == dec[r, c] * float(s[c // 128, r]), (r, c)

@@ -173,3 +173,56 @@ def test_bias_update_balances_a_skewed_router():
         spread.append(counts.max() / max(counts.min(), 1))
         b = oracle.bias_update(b, counts, T, K, 0.02)
     assert spread[0] > 4 and np.mean(spread[-10:]) < spread[0] / 2
+
+
+# ---- router logits z = x . E^T ([book] ch. 7 "The router's affinity scores") ----------
+
+def test_router_logits_hand_worked_non_square():
+    # d = 5 channels, E = 3 centroids; every product and sum is exact in float32
+    x = np.array([[1, 2, 0, -1, 3], [0, 0, 4, 0, 0]], np.float32)
+    cen = np.array([[1, 0, 0, 0, 0], [0, 1, 1, 0, 0], [2, -1, 0, 1, 0.5]], np.float32)
+    z = oracle.router_logits(x, cen)
+    assert z.shape == (2, 3) and z.dtype == np.float32
+    # worked by hand: row 0: 1; 2 + 0; 2 - 2 + 0 - 1 + 1.5.  row 1: 0; 4; 0
+    assert z.tolist() == [[1.0, 2.0, 0.5], [0.0, 4.0, 0.0]]
+    # the operands are not interchangeable: [T, d] . [E, d]^T with T != E and d != E
+    try:
+        zz = oracle.router_logits(cen, x)
+    except ValueError:
+        zz = None
+    assert zz is None or zz.shape != z.shape
+
+
+def test_router_logits_one_hot_rows_pick_centroid_entries():
+    rng = np.random.default_rng(3)
+    E, d = 16, 384
+    cen = (rng.standard_normal((E, d)) * 0.02).astype(np.float32)
+    chans = np.array([0, 5, 127, 128, 383])
+    x = np.zeros((len(chans), d), np.float32)
+    x[np.arange(len(chans)), chans] = 1.0
+    z = oracle.router_logits(x, cen)
+    assert np.array_equal(z, cen[:, chans].T)            # exactly the centroid entries
+
+
+def test_router_logits_constant_row_is_scaled_centroid_sum():
+    import math
+    rng = np.random.default_rng(4)
+    E, d = 8, 512
+    cen = (rng.standard_normal((E, d)) * 0.02).astype(np.float32)
+    alpha = 0.75
+    x = np.full((1, d), alpha, np.float32)
+    z = oracle.router_logits(x, cen)
+    want = np.array([math.fsum(alpha * float(v) for v in cen[i]) for i in range(E)])
+    # fsum is the exact sum; the oracle rounds its float64 sum once to float32
+    assert np.allclose(z[0], want.astype(np.float32), rtol=2 ** -22, atol=0)
+
+
+def test_router_logits_additive_in_x():
+    rng = np.random.default_rng(5)
+    E, d = 4, 256
+    # small integers: every product and partial sum is exact
+    cen = rng.integers(-8, 9, (E, d)).astype(np.float32)
+    x1 = rng.integers(-4, 5, (3, d)).astype(np.float32)
+    x2 = rng.integers(-4, 5, (3, d)).astype(np.float32)
+    assert np.array_equal(oracle.router_logits(x1 + x2, cen),
+                          oracle.router_logits(x1, cen) + oracle.router_logits(x2, cen))
