@@ -32,6 +32,7 @@ Modules:
   gemm     -- block-scaled GEMM with per-128-K promotion, SwiGLU expert, combine
   layer    -- the whole layer forward, and a per-token variant for large shapes
   balance  -- sequence-wise balance statistics f_i, P_i and the complementary loss
+  backward -- expert backward: Dgrad / Wgrad GEMMs, 128x1 regrouping, SwiGLU recompute
 
 Parity pins live in ``tests/test_oracle_*.py``.  Functions without an independent
 pin say "parity unpinned" in their docstring.
@@ -46,6 +47,8 @@ from .permute import permute
 from .gemm import blockscaled_gemm, swiglu_expert, combine
 from .layer import moe_layer, moe_layer_tokens
 from .balance import plain_topk, seq_balance_stats
+from .backward import (padded_offsets, quant_128x1_pow2_segments, wgrad, swiglu_backward,
+                       dequant_rows_1x128_f32, swiglu_cache, expert_backward)
 
 __all__ = [
     "E4M3_MAX", "E4M3_MIN_NORMAL", "e4m3_decode", "e4m3_decode_table", "e4m3_encode",
@@ -53,4 +56,6 @@ __all__ = [
     "dequant_128x128", "quant_1x128_pow2", "quant_128x128_pow2", "router_logits", "sigmoid_f32", "route", "route_token",
     "bias_update", "permute", "blockscaled_gemm", "swiglu_expert", "combine",
     "moe_layer", "moe_layer_tokens", "plain_topk", "seq_balance_stats",
+    "padded_offsets", "quant_128x1_pow2_segments", "wgrad", "swiglu_backward",
+    "dequant_rows_1x128_f32", "swiglu_cache", "expert_backward",
 ]
