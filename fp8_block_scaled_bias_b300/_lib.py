@@ -38,6 +38,10 @@ SIGNATURES = {
     "fp8_blockscaled_grouped_gemm": (_I, [_P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P, _I,
                                           _P, _P, _SZ, _P]),
     "fp8_grouped_gemm_ws_bytes": (_SZ, [_I, _I, _I]),
+    "moe_set_gemm_tiling": (_I, [_I]),
+    "moe_get_gemm_tiling": (_I, []),
+    "moe_test_gemm_wait_expiry": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _I, _P,
+                                       C.c_ulonglong, _P]),
     "moe_swiglu_fp8_fwd": (_I, [_P, _P, _I, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P,
                                 _P, _P, _SZ, _P]),
     "moe_swiglu_ws_bytes": (_SZ, [_I, _I, _I]),

@@ -246,6 +246,33 @@ int fp8_blockscaled_grouped_gemm(const uint8_t* A, const float* sA, int M_a,
   return moe::launch_fp8_gemm(a, moe::kEpiBF16, s);
 }
 
+int moe_set_gemm_tiling(int mode) {
+  if (mode < 0 || mode > 2) return MOE_ERR_INVALID_ARG;
+  moe::set_gemm_tiling(mode);
+  return MOE_OK;
+}
+
+int moe_get_gemm_tiling(void) { return moe::gemm_tiling(); }
+
+int moe_test_gemm_wait_expiry(const uint8_t* A, const float* sA, const uint8_t* B,
+                              const float* sB, const int32_t* seg_offsets, int G, int M, int N,
+                              int K, uint16_t* C, int ldc, int32_t* dev_status,
+                              unsigned long long wait_ns, void* stream) {
+  int st = check_gemm_dims(G, M, N, K);
+  if (st != MOE_OK) return st;
+  if (M == 0) return MOE_OK;
+  if (!A || !sA || !B || !sB || !seg_offsets || !C || !dev_status) return MOE_ERR_INVALID_ARG;
+  if (ldc < N || ldc % 8 != 0 || !aligned16(A) || !aligned16(B) || !aligned16(C))
+    return MOE_ERR_INVALID_ARG;
+  if (wait_ns < 100000ull || wait_ns > 2000000000ull) return MOE_ERR_INVALID_ARG;
+  GemmArgs a{};
+  a.A = A; a.sA = sA; a.B = B; a.sB = sB; a.seg = seg_offsets;
+  a.G = G; a.M = M; a.N = N; a.K = K; a.C = C; a.ldc = ldc; a.status = dev_status;
+  a.wait_ns = wait_ns;
+  a.stall = 1;
+  return moe::launch_fp8_gemm(a, moe::kEpiBF16, as_stream(stream));
+}
+
 // ---- experts -------------------------------------------------------------------------
 
 size_t moe_swiglu_ws_bytes(int rows, int d, int f) {

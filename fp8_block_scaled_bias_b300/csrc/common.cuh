@@ -69,17 +69,37 @@ MOE_DEV bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Same, with cluster-scope acquire: for barriers that the other CTA of a pair arrives on.
+MOE_DEV bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait until the phase with `parity` has completed.  Returns false (after setting
 // *abort and the status word) if the wait exceeds kWaitLimitNs, or if another thread
 // of the block has already aborted.
-MOE_DEV bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, int32_t* status) {
-  if (mbar_try_wait(bar, parity)) return true;
+// CLUSTER: cluster-scope acquire (the barrier receives arrivals from the other CTA of a
+// pair).  limit_ns: the wait limit (kWaitLimitNs unless a caller asks for less).
+template <bool CLUSTER = false>
+MOE_DEV bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, int32_t* status,
+                       uint64_t limit_ns = kWaitLimitNs) {
+  auto poll = [&]() {
+    return CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+  };
+  if (poll()) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (poll()) return true;
     if ((i & 255u) == 0) {
       if (*abort) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         *abort = 1;
         set_status(status, MOE_ERR_DEVICE_TIMEOUT);
         return false;
@@ -90,9 +110,11 @@ MOE_DEV bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, int32
 
 // Warp-wide wait: lane 0 polls the barrier (the other lanes do not compete for shared
 // memory while they wait), then the warp resynchronises.  All lanes get the result.
-MOE_DEV bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort, int32_t* status) {
+template <bool CLUSTER = false>
+MOE_DEV bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort, int32_t* status,
+                            uint64_t limit_ns = kWaitLimitNs) {
   int ok = 1;
-  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort, status) ? 1 : 0;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait<CLUSTER>(bar, parity, abort, status, limit_ns) ? 1 : 0;
   ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
   return ok != 0;
 }
@@ -123,17 +145,6 @@ MOE_DEV void tma_load_2d_hint(uint32_t dst, const void* tmap, int32_t x, int32_t
       : "memory");
 }
 
-// Same box, written to the same shared-memory offset in every CTA of `cta_mask` in the
-// cluster; each destination CTA's mbarrier at offset `bar` receives the bytes it got.
-MOE_DEV void tma_load_2d_multicast(uint32_t dst, const void* tmap, int32_t x, int32_t y,
-                                   uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "h"(cta_mask)
-      : "memory");
-}
-
 // ---- cp.async (per-thread asynchronous global -> shared copies) ----------------------------
 
 MOE_DEV void cp_async_4(uint32_t dst, const void* src) {
@@ -142,21 +153,21 @@ MOE_DEV void cp_async_4(uint32_t dst, const void* src) {
 
 MOE_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 
+// Arrive on `bar` once every cp.async this thread issued so far has landed (the barrier's
+// expected count includes this arrival: .noinc).
+MOE_DEV void cp_async_mbar_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 // Wait until at most N of this thread's committed groups are still in flight.
 template <int N>
 MOE_DEV void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-// ---- thread-block clusters -------------------------------------------------------------
+// ---- CTA pairs (clusters of two CTAs sharing one tcgen05 MMA) -------------------------
 
 MOE_DEV uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-MOE_DEV uint32_t cluster_nctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
   return r;
 }
 
@@ -172,10 +183,41 @@ MOE_DEV uint32_t ncluster_x() {
   return r;
 }
 
-// All threads of all CTAs of the cluster (release/acquire ordering of shared memory).
+// All threads of both CTAs of the cluster (release/acquire ordering of shared memory).
 MOE_DEV void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
                ::: "memory");
+}
+
+// The shared::cluster address of the object at shared::cta address `a` in CTA `rank`.
+MOE_DEV uint32_t mapa_shared(uint32_t a, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+  return r;
+}
+
+// Arrive on an mbarrier that may sit in the other CTA of the pair (cluster-scope release).
+MOE_DEV void mbar_arrive_cluster(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+               : "memory");
+}
+
+MOE_DEV void mbar_arrive_expect_tx_cluster(uint32_t cluster_bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(
+                   cluster_bar),
+               "r"(bytes)
+               : "memory");
+}
+
+// 2-D tiled load into this CTA's shared memory whose completion (transaction bytes) is
+// signalled on an mbarrier of either CTA of the pair.
+MOE_DEV void tma_load_2d_pair(uint32_t dst, const void* tmap, int32_t x, int32_t y,
+                              uint32_t cluster_bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(cluster_bar)
+      : "memory");
 }
 
 MOE_DEV uint64_t policy_evict_first() {
@@ -267,15 +309,6 @@ MOE_DEV void mma_commit(uint32_t bar) {
       : "memory");
 }
 
-// Arrive once on the mbarrier at offset `bar` of every CTA in `cta_mask` when every MMA
-// issued so far by this thread has completed.
-MOE_DEV void mma_commit_multicast(uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar), "h"(cta_mask)
-      : "memory");
-}
-
 // Warp-wide: 32 lanes x 32 consecutive FP32 columns from TMEM (lane window set by the
 // warp's rank within its warpgroup).
 MOE_DEV void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
@@ -347,6 +380,21 @@ MOE_DEV uint32_t pack_bf16x2(float lo, float hi) {
 // The scale of a 1x128 / 128x128 group: amax / 448, correctly rounded; 1 for amax 0.
 MOE_DEV float e4m3_scale_from_amax(float amax) {
   return amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f);
+}
+
+// Power-of-two scale rule (the MX-native variant and the 128x1 backward tiles): the
+// smallest s = 2^k with 448 * s >= amax, found exactly from amax's exponent and mantissa
+// (448 = 1.75 * 2^8), at least 2^-126; s = 1 for amax == 0.  Division by it is exact.
+MOE_DEV float pow2_scale_from_amax(float amax) {
+  if (amax == 0.0f) return 1.0f;
+  uint32_t b = __float_as_uint(amax);
+  int e = static_cast<int>((b >> 23) & 0xFFu) - 127;
+  if (((b >> 23) & 0xFFu) == 0) {                         // subnormal amax: rescale exactly
+    b = __float_as_uint(amax * 18446744073709551616.0f);  // * 2^64
+    e = static_cast<int>((b >> 23) & 0xFFu) - 127 - 64;
+  }
+  const int k = max(e - 8 + ((b & 0x7FFFFFu) > 0x600000u ? 1 : 0), -126);
+  return __uint_as_float(static_cast<uint32_t>(k + 127) << 23);
 }
 
 }  // namespace moe

@@ -12,31 +12,39 @@
 // into one of two TMEM buffers while the epilogue warps fold the other into FP32
 // registers.
 //
-// Kernel shape (one CTA per SM, persistent, in clusters of cs = 1, 2 or 4 CTAs):
-//   warp 0      TMA producer: A tile 128x128 and B tile 256x128 (FP8) per K block,
-//               4 stages.  The cs CTAs of a cluster work
-//               on neighbouring N tiles of the same row block, so they need the same A
-//               tile: each loads 128/cs of its rows and multicasts them to all, which
-//               divides the A traffic from L2 by cs.
-//   warp 1      TMEM allocation; one thread issues 4 MMAs (M128 N256 K32) per K block
-//               into TMEM buffer (kb mod 2) and commits to the buffer barrier and to the
-//               stage barrier of every CTA of the cluster (a stage is refilled only when
-//               all cs CTAs have consumed it).  This warp never touches shared memory in
-//               its loop: on this tensor core a shared-memory access by the issuing warp
-//               (an mbarrier wait included) waits behind the operand reads of its MMAs in
-//               flight and leaves the pipe idle.
+// Two tilings of the same kernel (one CTA per SM, persistent):
+//   single  one CTA per 128-row x 256-column tile: per K block it loads A 128x128 and
+//           B 256x128 (48 KB) and issues M128 N256 MMAs (tcgen05 cta_group::1).
+//   pair    two CTAs (a cluster of 2) per 256-row x 256-column tile: one tcgen05
+//           cta_group::2 MMA (M256 N256) reads A rows [0, 128) and B rows [0, 128) from
+//           the first CTA's shared memory and A rows [128, 256), B rows [128, 256) from
+//           the second's, and writes rows [0, 128) of the accumulator into the first
+//           CTA's TMEM and rows [128, 256) into the second's.  Each CTA loads 32 KB per K
+//           block for the same MMA work per SM, so a third fewer bytes ride the L2 ->
+//           shared-memory path that bounds the single tiling.  Each CTA still promotes
+//           its own 128 rows.
+// Warp roles:
+//   warp 0      TMA producer of this CTA's A and B rows, STAGES-deep ring.  In the pair
+//               tiling both CTAs' loads complete on the first CTA's stage barrier.
+//   warp 1      TMEM allocation; one thread issues 4 MMAs (K32 each) per K block into
+//               TMEM buffer (kb mod 2) and commits to the stage and buffer barriers (of
+//               both CTAs in the pair tiling; only the first CTA issues).  This warp
+//               never touches shared memory in its loop: on this tensor core a shared-
+//               memory access by the issuing warp (an mbarrier wait included) waits
+//               behind the operand reads of its MMAs in flight and leaves the pipe idle.
 //   warp 10     MMA scheduler: waits on the stage and TMEM-buffer mbarriers for each K
 //               block and releases warp 1 through a named barrier (lockstep; its OR-
 //               reduction carries an abort, so both warps leave the loop together)
 //   warps 2..9  promotion + epilogue: warp w reads TMEM lanes 32*(w%4).. (its rows);
 //               warps 2-5 own 128 of the 256 columns, warps 6-9 the other 128.  Each
 //               thread adds its partials into 128 FP32 accumulators with packed FMAs,
-//               16 columns per TMEM load; the scales arrive through cp.async rings.
-// Tiles are 128 rows x 256 columns; the per-K-block synchronisation costs about the
-// same for any tile width, so the wider tile amortises it over twice the MMA work.  The tile list walks segments in order, then N
-// tiles, with the M tiles of a segment fastest so CTAs working at the same time share
-// the expert's weight tile through L2.  Segments need not be multiples of 128 rows:
-// rows past a segment's end are computed and not stored.
+//               16 columns per TMEM load; the scales arrive through per-thread cp.async
+//               rings SPF K blocks ahead (measured faster on this B300 than a separate
+//               feeder warp with an mbarrier-tracked ring).
+// The tile list walks segments in order, then N tiles, with the M tiles of a segment
+// fastest so CTAs working at the same time share the expert's weight tile through L2.
+// Segments need not be multiples of the tile height: rows past a segment's end are
+// computed and not stored.
 //
 // Epilogues:
 //   kEpiBF16    C = BF16(acc)
@@ -46,7 +54,13 @@
 //               thread holds 64 gate and the 64 matching up accumulators of its row:
 //               h = silu(gate) * up.  The two threads of a row exchange their max-abs
 //               through shared memory and requantise h -> hq (E4M3) and sh (FP32).
+//
+// Every mbarrier wait is bounded (GemmParams::wait_ns); on expiry the kernel records
+// MOE_ERR_DEVICE_TIMEOUT, stops issuing work, lets its copies and MMAs in flight land,
+// frees TMEM and returns.
+#include <atomic>
 #include <cuda.h>
+#include <mutex>
 
 #include "common.cuh"
 #include "launch.h"
@@ -54,10 +68,9 @@
 namespace moe {
 
 namespace gk {
-constexpr int BM = 128, BN = 256, BK = 128;
-constexpr int A_BYTES = BM * BK;
-constexpr int B_BYTES = BN * BK;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int BN = 256, BK = 128;
+constexpr int ROWS = 128;                          // accumulator rows per CTA (TMEM lanes)
+constexpr int A_BYTES = ROWS * BK;
 constexpr int EPI_WARPS = 8;
 constexpr int EPI_THREADS = EPI_WARPS * 32;
 constexpr int SCHED_WARP = 2 + EPI_WARPS;          // waits on barriers for the MMA warp
@@ -65,25 +78,27 @@ constexpr int THREADS = 64 + EPI_THREADS + 32;
 constexpr int MMA_BAR = 1;                         // named barrier: MMA warp + scheduler
 constexpr int SPF = 8;                             // K blocks of scales prefetched ahead
 constexpr int MAX_G = 1024;
-constexpr int TBUF = 2;                  // TMEM partial buffers of BN columns
+constexpr int TBUF = 2;                            // TMEM partial buffers of BN columns
 constexpr uint32_t TMEM_COLS = 512;
 
-template <int EPI>
+template <bool PAIR>
 struct Layout {
-  static constexpr int STAGES = 4;
-  static constexpr int STASH = 0;
+  static constexpr int BM = PAIR ? 2 * ROWS : ROWS;     // rows per work unit
+  static constexpr int B_ROWS = PAIR ? BN / 2 : BN;     // B rows this CTA loads
+  static constexpr int B_BYTES = B_ROWS * BK;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES; // bytes this CTA loads per K block
+  static constexpr int STAGES = PAIR ? 6 : 4;
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
-  static constexpr int OFF_STASH = OFF_B + STAGES * B_BYTES;
-  static constexpr int OFF_BAR = OFF_STASH + STASH;
-  // barriers: full[STAGES], empty[STAGES], tfull[TBUF], tempty[TBUF], amax[2], drain
-  static constexpr int NUM_BARS = 2 * STAGES + 2 * TBUF + 3;
+  static constexpr int OFF_BAR = OFF_B + STAGES * B_BYTES;
+  // barriers: full[STAGES], empty[STAGES], tfull[TBUF], tempty[TBUF], amax[2], drain, stall
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * TBUF + 4;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;   // tmem slot, abort, total, bad
   static constexpr int OFF_SEG = OFF_MISC + 16;
   static constexpr int OFF_TSTART = OFF_SEG + (MAX_G + 1) * 4;
   static constexpr int OFF_AMAX = OFF_TSTART + (MAX_G + 1) * 4;   // [2 bufs][2 groups][128]
   // per-thread rings of prefetched scales: sA [SPF][EPI_THREADS], sB [SPF][EPI_WARPS][2]
-  static constexpr int OFF_SCALE_A = OFF_AMAX + 2 * 2 * BM * 4;
+  static constexpr int OFF_SCALE_A = OFF_AMAX + 2 * 2 * ROWS * 4;
   static constexpr int OFF_SCALE_B = OFF_SCALE_A + SPF * EPI_THREADS * 4;
   static constexpr int SMEM_USED = OFF_SCALE_B + SPF * EPI_WARPS * 2 * 4;
   static constexpr int SMEM_ALLOC = SMEM_USED + 1024;              // 1024-B alignment slack
@@ -101,6 +116,8 @@ struct GemmParams {
   uint8_t* hq;
   float* sh;
   int32_t* status;
+  uint64_t wait_ns;      // limit of every mbarrier wait
+  int stall;             // != 0: the scheduler waits on a barrier nothing arrives on
 };
 
 namespace {
@@ -109,11 +126,12 @@ namespace {
 // h is compared with the oracle's float64 silu within a tolerance, never bit for bit)
 MOE_DEV float silu_f32(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
-// Cluster work unit -> (segment, first row, valid rows, unit index within the row
-// block).  ustart[g] = first unit of segment g (non-decreasing); the largest g with
-// ustart[g] <= unit is non-empty.  Units of a segment run M blocks fastest.
+// Work unit -> (segment, first row of the unit, N tile).  ustart[g] = first unit of
+// segment g (non-decreasing); the largest g with ustart[g] <= unit is non-empty.  Units
+// of a segment run M blocks (of BM rows) fastest.
+template <int BM>
 MOE_DEV void decode_unit(int unit, const int* ustart, const int* seg, int G, int& g, int& m0,
-                         int& rows_valid, int& nu) {
+                         int& nt) {
   int lo = 0, hi = G - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -122,19 +140,17 @@ MOE_DEV void decode_unit(int unit, const int* ustart, const int* seg, int G, int
   }
   g = lo;
   const int cnt = seg[g + 1] - seg[g];
-  const int mt = (cnt + gk::BM - 1) / gk::BM;
+  const int mt = (cnt + BM - 1) / BM;
   const int local = unit - ustart[g];
-  const int m = local % mt;
-  nu = local / mt;
-  m0 = seg[g] + m * gk::BM;
-  rows_valid = min(gk::BM, seg[g + 1] - m0);
+  nt = local / mt;
+  m0 = seg[g] + (local % mt) * BM;
 }
 
 // Bounded wait used only while shutting down after an abort: ignores the abort flag.
-MOE_DEV void mbar_drain(uint32_t bar, uint32_t parity) {
+MOE_DEV void mbar_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > kWaitLimitNs) return;
+    if (globaltimer_ns() - t0 > limit_ns) return;
   }
 }
 
@@ -147,16 +163,64 @@ MOE_DEV uint32_t e4m3x4(float a, float b, float c, float d, float rs) {
   return lo | (hi << 16);
 }
 
+// ---- tcgen05 forms of the two tilings (one kernel uses one cta_group throughout) ----
+
+template <bool PAIR>
+MOE_DEV void tmem_alloc_g(uint32_t dst, uint32_t ncols) {
+  if (PAIR) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  } else {
+    tmem_alloc(dst, ncols);
+  }
+}
+
+template <bool PAIR>
+MOE_DEV void tmem_dealloc_g(uint32_t taddr, uint32_t ncols) {
+  if (PAIR)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+  else
+    tmem_dealloc(taddr, ncols);
+}
+
+template <bool PAIR>
+MOE_DEV void mma_fp8_g(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                       uint32_t accumulate) {
+  if (PAIR)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  else
+    mma_f8f6f4(d_tmem, adesc, bdesc, idesc, accumulate);
+}
+
+// Arrive once on the mbarrier at shared::cluster address `bar` (either CTA of the pair)
+// when every MMA issued so far by this thread has completed.
+template <bool PAIR>
+MOE_DEV void mma_commit_g(uint32_t bar) {
+  if (PAIR)
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+  else
+    mma_commit(bar);
+}
+
 }  // namespace
 
-template <int EPI>
+template <int EPI, bool PAIR>
 __global__ void __launch_bounds__(gk::THREADS, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
   using namespace gk;
-  using L = Layout<EPI>;
-  constexpr int STAGES = L::STAGES;
-  constexpr int TPU = 1;                             // N tiles per work unit
+  using L = Layout<PAIR>;
+  constexpr int STAGES = L::STAGES, BM = L::BM;
   extern __shared__ uint8_t gemm_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(gemm_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -168,6 +232,7 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
   auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + TBUF + b); };
   auto amax_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 * TBUF + b); };
   const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 2 * TBUF + 2);
+  const uint32_t stall_bar = bar0 + 8u * (2 * STAGES + 2 * TBUF + 3);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
   int* total_units = reinterpret_cast<int*>(smem + L::OFF_MISC + 8);
@@ -179,12 +244,11 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = p.G;
   const int NT = (p.N + BN - 1) / BN;      // N tiles (the last may be half-filled)
-  const int cs = static_cast<int>(cluster_nctarank());
-  const int crank = static_cast<int>(cluster_ctarank());
-  const int NU = NT / TPU / cs;            // cluster work units per M block
   const int KB = p.K / BK;
-  const uint16_t cmask = static_cast<uint16_t>((1u << cs) - 1u);
-  const int a_rows = BM / cs;              // A rows this CTA loads and multicasts
+  const uint64_t wait_ns = p.wait_ns;
+  // pair tiling: rank 0 issues the MMAs and owns the stage barriers; rank 1 is its peer
+  const uint32_t crank = PAIR ? cluster_ctarank() : 0u;
+  const bool issuer = crank == 0;
 
   // ---- segment table and unit prefix (every CTA computes its own copy) ----
   if (tid == 0) { *abort_flag = 0; *bad = 0; }
@@ -198,7 +262,7 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
     for (int g = g0; g < g1; ++g) {
       const int cnt = seg[g + 1] - seg[g];
       if (cnt < 0) *bad = 1;
-      local += (max(cnt, 0) + BM - 1) / BM * NU;
+      local += (max(cnt, 0) + BM - 1) / BM * NT;
     }
     if (tid == 0 && (seg[0] != 0 || seg[G] > p.M)) *bad = 1;
     int incl = local;
@@ -215,7 +279,7 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
     int run = wbase + incl - local;
     for (int g = g0; g < g1; ++g) {
       ustart[g] = run;
-      run += (max(seg[g + 1] - seg[g], 0) + BM - 1) / BM * NU;
+      run += (max(seg[g + 1] - seg[g], 0) + BM - 1) / BM * NT;
     }
     if (tid == THREADS - 1) {
       int tot = 0;
@@ -225,6 +289,8 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
     }
   }
   __syncthreads();
+  // Both CTAs of a pair read the same segment table, so they leave here together,
+  // before either touches the other's shared memory.
   if (*bad) {
     if (tid == 0) set_status(p.status, MOE_ERR_DEVICE_DATA);
     return;
@@ -232,21 +298,32 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
   const int total = *total_units;
 
   if (tid == 0) {
-    for (int s = 0; s < STAGES; ++s) { mbar_init(full_bar(s), 1); mbar_init(empty_bar(s), cs); }
-    for (int b = 0; b < TBUF; ++b) { mbar_init(tfull_bar(b), 1); mbar_init(tempty_bar(b), EPI_WARPS); }
+    // full: one arrival per loading CTA (plus the bytes); empty: one MMA commit;
+    // tempty: every promotion warp of the CTA(s) sharing the accumulator
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), PAIR ? 2 : 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < TBUF; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), (PAIR ? 2 : 1) * EPI_WARPS);
+    }
     for (int b = 0; b < 2; ++b) mbar_init(amax_bar(b), EPI_THREADS);
     mbar_init(drain_bar, 1);
+    mbar_init(stall_bar, 1);
     fence_barrier_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
   }
-  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+  if (warp == 1) tmem_alloc_g<PAIR>(smem_u32(tmem_slot), TMEM_COLS);
   tc_fence_before();
-  cluster_sync();          // every CTA's barriers exist before any multicast reaches it
+  if (PAIR) cluster_sync();   // both CTAs' barriers exist before either signals the other
+  else __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int first_unit = static_cast<int>(cluster_id_x());
-  const int unit_stride = static_cast<int>(ncluster_x());
+  const int first_unit = PAIR ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
+  const int unit_stride = PAIR ? static_cast<int>(ncluster_x()) : static_cast<int>(gridDim.x);
+  const int row_off = static_cast<int>(crank) * ROWS;   // this CTA's rows within the unit
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -254,39 +331,47 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
       uint32_t it = 0;
       bool ok = true;
       for (int unit = first_unit; ok && unit < total; unit += unit_stride) {
-        int g, m0, rv, cu;
-        decode_unit(unit, ustart, seg, G, g, m0, rv, cu);
-        const int nu = cu * cs + crank;
-        for (int t = 0; ok && t < TPU; ++t) {
-          const int brow = g * p.N + (nu * TPU + t) * BN;
-          for (int kb = 0; kb < KB; ++kb, ++it) {
-            const int s = it % STAGES;
-            const uint32_t ph = (it / STAGES) & 1;
-            if (!mbar_wait(empty_bar(s), ph ^ 1, abort_flag, p.status)) { ok = false; break; }
-            mbar_arrive_expect_tx(full_bar(s), STAGE_BYTES);   // whole A tile + own B tile
-            const uint32_t a_dst = sbase + L::OFF_A + s * A_BYTES;
-            if (cs == 1)
-              tma_load_2d(a_dst, &tmA, kb * BK, m0, full_bar(s));
-            else
-              tma_load_2d_multicast(a_dst + crank * a_rows * BK, &tmA, kb * BK,
-                                    m0 + crank * a_rows, full_bar(s), cmask);
-            tma_load_2d(sbase + L::OFF_B + s * B_BYTES, &tmB, kb * BK, brow, full_bar(s));
+        int g, m0, nt;
+        decode_unit<BM>(unit, ustart, seg, G, g, m0, nt);
+        const int arow = m0 + row_off;
+        const int brow = g * p.N + nt * BN + static_cast<int>(crank) * L::B_ROWS;
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (!mbar_wait<PAIR>(empty_bar(s), ph ^ 1, abort_flag, p.status, wait_ns)) {
+            ok = false;
+            break;
+          }
+          const uint32_t a_dst = sbase + L::OFF_A + s * A_BYTES;
+          const uint32_t b_dst = sbase + L::OFF_B + s * L::B_BYTES;
+          if (PAIR) {
+            const uint32_t fb = mapa_shared(full_bar(s), 0);
+            mbar_arrive_expect_tx_cluster(fb, L::STAGE_BYTES);
+            tma_load_2d_pair(a_dst, &tmA, kb * BK, arow, fb);
+            tma_load_2d_pair(b_dst, &tmB, kb * BK, brow, fb);
+          } else {
+            mbar_arrive_expect_tx(full_bar(s), L::STAGE_BYTES);
+            tma_load_2d(a_dst, &tmA, kb * BK, arow, full_bar(s));
+            tma_load_2d(b_dst, &tmB, kb * BK, brow, full_bar(s));
           }
         }
       }
-      if (!ok) {
+      if (!ok && issuer) {
         // let the copies already issued land before the CTA's shared memory is released
+        // (the second CTA of a pair gives up only after a full wait limit without
+        // progress, long after its last copies landed)
         const uint32_t first = it > STAGES ? it - STAGES : 0;
-        for (uint32_t i = first; i < it; ++i) mbar_drain(full_bar(i % STAGES), (i / STAGES) & 1);
+        for (uint32_t i = first; i < it; ++i)
+          mbar_drain(full_bar(i % STAGES), (i / STAGES) & 1, wait_ns);
       }
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer (no shared-memory access in the loop) ----------------
-    constexpr uint32_t idesc = make_idesc(BM, BN, 0u, 0u);   // E4M3 x E4M3 -> F32
-    uint32_t it = 0;
-    bool ok = true;
-    for (int unit = first_unit; ok && unit < total; unit += unit_stride) {
-      for (int t = 0; ok && t < TPU; ++t) {
+    if (issuer) {
+      constexpr uint32_t idesc = make_idesc(BM, BN, 0u, 0u);   // E4M3 x E4M3 -> F32
+      uint32_t it = 0;
+      bool ok = true;
+      for (int unit = first_unit; ok && unit < total; unit += unit_stride) {
         for (int kb = 0; kb < KB; ++kb, ++it) {
           // released by the scheduler once stage s is full and TMEM buffer b is free
           if (named_bar_sync_or(MMA_BAR, 64, false)) { ok = false; break; }
@@ -295,32 +380,38 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
             const int b = it % TBUF;
             tc_fence_after();
             const uint64_t adesc = smem_desc_sw128(sbase + L::OFF_A + s * A_BYTES);
-            const uint64_t bdesc = smem_desc_sw128(sbase + L::OFF_B + s * B_BYTES);
+            const uint64_t bdesc = smem_desc_sw128(sbase + L::OFF_B + s * L::B_BYTES);
             const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
 #pragma unroll
             for (int k = 0; k < BK / 32; ++k)   // K = 32 bytes per MMA: +2 in the >>4 address
-              mma_f8f6f4(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, k > 0 ? 1u : 0u);
-            if (cs == 1) mma_commit(empty_bar(s));
-            else mma_commit_multicast(empty_bar(s), cmask);
-            mma_commit(tfull_bar(b));
+              mma_fp8_g<PAIR>(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, k > 0 ? 1u : 0u);
+            if (PAIR) {
+              mma_commit_g<true>(mapa_shared(empty_bar(s), 0));
+              mma_commit_g<true>(mapa_shared(empty_bar(s), 1));
+              mma_commit_g<true>(mapa_shared(tfull_bar(b), 0));
+              mma_commit_g<true>(mapa_shared(tfull_bar(b), 1));
+            } else {
+              mma_commit(empty_bar(s));
+              mma_commit(tfull_bar(b));
+            }
           }
           __syncwarp();
         }
       }
+      // every MMA issued so far must finish before TMEM is released
+      if (lane == 0) {
+        mma_commit_g<PAIR>(drain_bar);
+        mbar_drain(drain_bar, 0, wait_ns);
+      }
+      __syncwarp();
     }
-    // every MMA issued so far must finish before TMEM is released
-    if (lane == 0) {
-      mma_commit(drain_bar);
-      mbar_drain(drain_bar, 0);
-    }
-    __syncwarp();
   } else if (warp == SCHED_WARP) {
     // ---------------- MMA scheduler ----------------
     // Same iteration sequence as the MMA warp; one named barrier per K block.
-    uint32_t it = 0;
-    bool ok = true;
-    for (int unit = first_unit; ok && unit < total; unit += unit_stride) {
-      for (int t = 0; ok && t < TPU; ++t) {
+    if (issuer) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int unit = first_unit; ok && unit < total; unit += unit_stride) {
         for (int kb = 0; kb < KB; ++kb, ++it) {
           int good = 1;
           if (lane == 0) {
@@ -328,8 +419,10 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
             const uint32_t ph = (it / STAGES) & 1;
             const int b = it % TBUF;
             const uint32_t bph = (it / TBUF) & 1;
-            good = mbar_wait(tempty_bar(b), bph ^ 1, abort_flag, p.status) &&
-                   mbar_wait(full_bar(s), ph, abort_flag, p.status);
+            // failure-path test: a barrier nothing arrives on
+            good = (!p.stall || mbar_wait(stall_bar, 0, abort_flag, p.status, wait_ns)) &&
+                   mbar_wait<PAIR>(tempty_bar(b), bph ^ 1, abort_flag, p.status, wait_ns) &&
+                   mbar_wait<PAIR>(full_bar(s), ph, abort_flag, p.status, wait_ns);
           }
           good = __shfl_sync(0xFFFFFFFFu, good, 0);
           tc_fence_before();
@@ -339,44 +432,41 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
     }
   } else if (warp >= 2 && warp < 2 + EPI_WARPS) {
     // ---------------- promotion + epilogue ----------------
-    const int etid = tid - 64;
     const int grp = (warp - 2) >> 2;    // column half of the tile
     const int q = warp & 3;             // TMEM lane window
-    const int row = q * 32 + lane;      // row within the tile
+    const int row = q * 32 + lane;      // row within this CTA's 128 rows
     const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
+    const int etid = tid - 64;
     const int NB = p.N / 128;           // weight-scale rows per segment
-    // TMEM columns of this thread's eight 16-column chunks (SwiGLU: 4 gate then 4 up)
-    int cols[8];
-#pragma unroll
-    for (int c = 0; c < 8; ++c)
-      cols[c] = (EPI == kEpiSwiGLU) ? grp * 128 + (c < 4 ? 0 : 64) + (c & 3) * 16
-                                    : grp * 128 + c * 16;
+    // the arrival that releases a TMEM buffer goes to the MMA-issuing CTA
+    const uint32_t tempty_dst[TBUF] = {PAIR ? mapa_shared(tempty_bar(0), 0) : tempty_bar(0),
+                                       PAIR ? mapa_shared(tempty_bar(1), 0) : tempty_bar(1)};
+    // TMEM columns of this thread's eight 16-column chunks, from its half's first column
+    // (SwiGLU: 4 gate then 4 up)
+    auto col_of = [](int c) {
+      return static_cast<uint32_t>((EPI == kEpiSwiGLU) ? (c < 4 ? 0 : 64) + (c & 3) * 16 : c * 16);
+    };
     // Scale prefetch: every K block needs sA[kb][row] (this thread's row) and the one or
     // two weight scales of the tile's N blocks.  They are copied into shared-memory rings
-    // SPF K blocks ahead with cp.async, following the same (unit, tile, K block) sequence
-    // as the promotion loop, so the L2 latency never sits on the critical path.
+    // SPF K blocks ahead with cp.async, following the same (unit, K block) sequence as
+    // the promotion loop, so the L2 latency never sits on the critical path.
     const uint32_t ring_a = sbase + L::OFF_SCALE_A + static_cast<uint32_t>(etid) * 4;
     const uint32_t ring_b = sbase + L::OFF_SCALE_B + static_cast<uint32_t>(warp - 2) * 8;
     const float* ring_a_f = reinterpret_cast<const float*>(smem + L::OFF_SCALE_A) + etid;
     const float* ring_b_f = reinterpret_cast<const float*>(smem + L::OFF_SCALE_B) + (warp - 2) * 2;
-    int pf_unit = first_unit, pf_t = 0, pf_kb = 0;       // prefetch cursor
-    int pf_g = 0, pf_m0 = 0, pf_nu = 0;
+    int pf_unit = first_unit, pf_kb = 0;                 // prefetch cursor
+    int pf_g = 0, pf_m0 = 0, pf_nt = 0;
     bool pf_live = pf_unit < total;
-    if (pf_live) {
-      int rv_unused, cu;
-      decode_unit(pf_unit, ustart, seg, G, pf_g, pf_m0, rv_unused, cu);
-      pf_nu = cu * cs + crank;
-    }
+    if (pf_live) decode_unit<BM>(pf_unit, ustart, seg, G, pf_g, pf_m0, pf_nt);
     uint32_t pf_it = 0;
     auto prefetch_one = [&]() {
       // issue the copies of the cursor's K block into ring slot pf_it % SPF, then advance
       if (pf_live) {
-        const int nt = pf_nu * TPU + pf_t;
         // (a half-filled last tile has no second N block: read a valid scale, unused)
-        const int nb0 = (EPI == kEpiSwiGLU) ? 2 * nt : min(2 * nt + grp, NB - 1);
-        const int nb1 = (EPI == kEpiSwiGLU) ? 2 * nt + 1 : nb0;
+        const int nb0 = (EPI == kEpiSwiGLU) ? 2 * pf_nt : min(2 * pf_nt + grp, NB - 1);
+        const int nb1 = (EPI == kEpiSwiGLU) ? 2 * pf_nt + 1 : nb0;
         const int slot = static_cast<int>(pf_it % SPF);
-        const int arow = min(pf_m0 + row, p.M - 1);
+        const int arow = min(pf_m0 + row_off + row, p.M - 1);
         cp_async_4(ring_a + slot * EPI_THREADS * 4,
                    p.sA + static_cast<long long>(pf_kb) * p.M + arow);
         if (lane == 0) {
@@ -386,16 +476,9 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
         }
         if (++pf_kb == KB) {
           pf_kb = 0;
-          if (++pf_t == TPU) {
-            pf_t = 0;
-            pf_unit += unit_stride;
-            pf_live = pf_unit < total;
-            if (pf_live) {
-              int rv_unused, cu;
-              decode_unit(pf_unit, ustart, seg, G, pf_g, pf_m0, rv_unused, cu);
-              pf_nu = cu * cs + crank;
-            }
-          }
+          pf_unit += unit_stride;
+          pf_live = pf_unit < total;
+          if (pf_live) decode_unit<BM>(pf_unit, ustart, seg, G, pf_g, pf_m0, pf_nt);
         }
       }
       cp_async_commit();                                 // one group per K block, maybe empty
@@ -411,100 +494,106 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
     int ucount = 0;
     bool ok = true;
     for (int unit = first_unit; ok && unit < total; unit += unit_stride, ++ucount) {
-      int g, m0, rv, cu;
-      decode_unit(unit, ustart, seg, G, g, m0, rv, cu);
-      const int nu = cu * cs + crank;
-      (void)g;
-      for (int t = 0; ok && t < TPU; ++t) {
-        const int nt = nu * TPU + t;
-        float2 acc2[64];
+      int g, m0, nt;
+      decode_unit<BM>(unit, ustart, seg, G, g, m0, nt);
+      const int r0 = m0 + row_off;                       // first row of this CTA's part
+      const int rv = min(ROWS, seg[g + 1] - r0);         // its valid rows (may be <= 0)
+      float2 acc2[64];
 #pragma unroll
-        for (int i = 0; i < 64; ++i) acc2[i] = make_float2(0.0f, 0.0f);
-        for (int kb = 0; kb < KB; ++kb, ++it) {
-          const float sa = nsa, sb0 = nsb0, sb1 = nsb1;
-          const int b = it % TBUF;
-          const uint32_t bph = (it / TBUF) & 1;
-          if (!mbar_wait_warp(tfull_bar(b), bph, abort_flag, p.status)) { ok = false; break; }
-          tc_fence_after();
-          const float sc0 = __fmul_rn(sa, sb0);
-          const float sc1 = __fmul_rn(sa, sb1);
-          const uint32_t tb = tmem_base + lane_addr + static_cast<uint32_t>(b * BN);
-          // two 16-column loads in flight per wait: four TMEM round trips per K block
-#pragma unroll
-          for (int c = 0; c < 8; c += 2) {
-            const float sc = (c < 4) ? sc0 : sc1;
-            const float2 sc2 = make_float2(sc, sc);
-            uint32_t v[2][16];
-            tmem_ld_32x32b_x16(tb + static_cast<uint32_t>(cols[c]), v[0]);
-            tmem_ld_32x32b_x16(tb + static_cast<uint32_t>(cols[c + 1]), v[1]);
-            tmem_ld_wait();
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-              for (int i = 0; i < 8; ++i)
-                acc2[(c + h) * 8 + i] = __ffma2_rn(
-                    sc2,
-                    make_float2(__uint_as_float(v[h][2 * i]), __uint_as_float(v[h][2 * i + 1])),
-                    acc2[(c + h) * 8 + i]);
-          }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(tempty_bar(b));     // the buffer is folded in
-          // scales of K block it + 1: their shared-memory latency overlaps the next wait
-          prefetch_one();                                // K block it + SPF - 1
-          cp_async_wait<SPF - 2>();                      // this thread's copies for it + 1
-          __syncwarp();                                  // lane 0's weight scales too
-          const int nslot = static_cast<int>((it + 1) % SPF);
-          nsa = ring_a_f[nslot * EPI_THREADS];
-          nsb0 = ring_b_f[nslot * EPI_WARPS * 2];
-          nsb1 = ring_b_f[nslot * EPI_WARPS * 2 + 1];
+      for (int i = 0; i < 64; ++i) acc2[i] = make_float2(0.0f, 0.0f);
+      for (int kb = 0; kb < KB; ++kb, ++it) {
+        const float sa = nsa, sb0 = nsb0, sb1 = nsb1;
+        const int b = it % TBUF;
+        const uint32_t bph = (it / TBUF) & 1;
+        if (!mbar_wait_warp<PAIR>(tfull_bar(b), bph, abort_flag, p.status, wait_ns)) {
+          ok = false;
+          break;
         }
-        if (!ok) break;
-        float* acc = reinterpret_cast<float*>(acc2);
+        tc_fence_after();
+        const float sc0 = __fmul_rn(sa, sb0);
+        const float sc1 = __fmul_rn(sa, sb1);
+        const uint32_t tb = tmem_base + lane_addr + static_cast<uint32_t>(b * BN + grp * 128);
+        // two 16-column loads in flight per wait: four TMEM round trips per K block
+#pragma unroll
+        for (int c = 0; c < 8; c += 2) {
+          uint32_t v[2][16];
+          tmem_ld_32x32b_x16(tb + col_of(c), v[0]);
+          tmem_ld_32x32b_x16(tb + col_of(c + 1), v[1]);
+          const float sc = (c < 4) ? sc0 : sc1;
+          const float2 sc2 = make_float2(sc, sc);
+          tmem_ld_wait();
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              acc2[(c + h) * 8 + i] = __ffma2_rn(
+                  sc2,
+                  make_float2(__uint_as_float(v[h][2 * i]), __uint_as_float(v[h][2 * i + 1])),
+                  acc2[(c + h) * 8 + i]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {                                 // the buffer is folded in
+          if (PAIR) mbar_arrive_cluster(tempty_dst[b]);
+          else mbar_arrive(tempty_dst[b]);
+        }
+        // scales of K block it + 1: their shared-memory latency overlaps the next wait
+        prefetch_one();                                  // K block it + SPF - 1
+        cp_async_wait<SPF - 2>();                        // this thread's copies for it + 1
+        __syncwarp();                                    // lane 0's weight scales too
+        const int nslot = static_cast<int>((it + 1) % SPF);
+        nsa = ring_a_f[nslot * EPI_THREADS];
+        nsb0 = ring_b_f[nslot * EPI_WARPS * 2];
+        nsb1 = ring_b_f[nslot * EPI_WARPS * 2 + 1];
+      }
+      if (!ok) break;
+      float* acc = reinterpret_cast<float*>(acc2);
 
-        if (EPI == kEpiBF16) {
-          if (row < rv && nt * BN + grp * 128 < p.N) {
-            uint4* dst = reinterpret_cast<uint4*>(p.C + static_cast<long long>(m0 + row) * p.ldc +
-                                                  nt * BN + grp * 128);
+      if (EPI == kEpiBF16) {
+        if (row < rv && nt * BN + grp * 128 < p.N) {
+          uint4* dst = reinterpret_cast<uint4*>(p.C + static_cast<long long>(r0 + row) * p.ldc +
+                                                nt * BN + grp * 128);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              uint4 o;
-              o.x = pack_bf16x2(acc[8 * j + 0], acc[8 * j + 1]);
-              o.y = pack_bf16x2(acc[8 * j + 2], acc[8 * j + 3]);
-              o.z = pack_bf16x2(acc[8 * j + 4], acc[8 * j + 5]);
-              o.w = pack_bf16x2(acc[8 * j + 6], acc[8 * j + 7]);
-              dst[j] = o;
-            }
+          for (int j = 0; j < 16; ++j) {
+            uint4 o;
+            o.x = pack_bf16x2(acc[8 * j + 0], acc[8 * j + 1]);
+            o.y = pack_bf16x2(acc[8 * j + 2], acc[8 * j + 3]);
+            o.z = pack_bf16x2(acc[8 * j + 4], acc[8 * j + 5]);
+            o.w = pack_bf16x2(acc[8 * j + 6], acc[8 * j + 7]);
+            dst[j] = o;
           }
-        } else {
-          // h = silu(gate) * up for this thread's 64 hidden columns
-          float amax = 0.0f;
+        }
+      } else {
+        // h = silu(gate) * up for this thread's 64 hidden columns
+        float amax = 0.0f;
 #pragma unroll
-          for (int i = 0; i < 64; ++i) {
-            acc[i] = __fmul_rn(silu_f32(acc[i]), acc[64 + i]);
-            amax = fmaxf(amax, fabsf(acc[i]));
-          }
-          const int buf = ucount & 1;
-          amax_x[(buf * 2 + grp) * BM + row] = amax;
-          mbar_arrive(amax_bar(buf));
-          if (!mbar_wait_warp(amax_bar(buf), (ucount >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
-          amax = fmaxf(amax, amax_x[(buf * 2 + (grp ^ 1)) * BM + row]);
-          const float s = e4m3_scale_from_amax(amax);
-          const float rs = __frcp_rn(s);
-          if (row < rv) {
-            const int f = p.N / 2;
-            uint4* dst = reinterpret_cast<uint4*>(p.hq + static_cast<long long>(m0 + row) * f +
-                                                  nt * 128 + grp * 64);
+        for (int i = 0; i < 64; ++i) {
+          acc[i] = __fmul_rn(silu_f32(acc[i]), acc[64 + i]);
+          amax = fmaxf(amax, fabsf(acc[i]));
+        }
+        const int buf = ucount & 1;
+        amax_x[(buf * 2 + grp) * ROWS + row] = amax;
+        mbar_arrive(amax_bar(buf));
+        if (!mbar_wait_warp(amax_bar(buf), (ucount >> 1) & 1, abort_flag, p.status, wait_ns)) {
+          ok = false;
+          break;
+        }
+        amax = fmaxf(amax, amax_x[(buf * 2 + (grp ^ 1)) * ROWS + row]);
+        const float s = e4m3_scale_from_amax(amax);
+        const float rs = __frcp_rn(s);
+        if (row < rv) {
+          const int f = p.N / 2;
+          uint4* dst = reinterpret_cast<uint4*>(p.hq + static_cast<long long>(r0 + row) * f +
+                                                nt * 128 + grp * 64);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const float* h = acc + 16 * j;
-              dst[j] = make_uint4(e4m3x4(h[0], h[1], h[2], h[3], rs),
-                                  e4m3x4(h[4], h[5], h[6], h[7], rs),
-                                  e4m3x4(h[8], h[9], h[10], h[11], rs),
-                                  e4m3x4(h[12], h[13], h[14], h[15], rs));
-            }
-            if (grp == 0) p.sh[static_cast<long long>(nt) * p.M + m0 + row] = s;
+          for (int j = 0; j < 4; ++j) {
+            const float* h = acc + 16 * j;
+            dst[j] = make_uint4(e4m3x4(h[0], h[1], h[2], h[3], rs),
+                                e4m3x4(h[4], h[5], h[6], h[7], rs),
+                                e4m3x4(h[8], h[9], h[10], h[11], rs),
+                                e4m3x4(h[12], h[13], h[14], h[15], rs));
           }
+          if (grp == 0) p.sh[static_cast<long long>(nt) * p.M + r0 + row] = s;
         }
       }
     }
@@ -512,10 +601,11 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
   }
 
   tc_fence_before();
-  cluster_sync();          // no CTA leaves while a cluster peer may still write into it
+  if (PAIR) cluster_sync();   // neither CTA leaves while the other may still signal it
+  else __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    tmem_dealloc_g<PAIR>(tmem_base, TMEM_COLS);
   }
 }
 
@@ -527,75 +617,111 @@ bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* ptr
 
 namespace {
 
-// Largest cluster size in {4, 2, 1} that divides the work units of one row block.
-int pick_cluster(int units_per_block) {
-  // Clusters share the A tile through multicast, which cuts L2 traffic but not the
-  // shared-memory traffic that bounds this kernel, and 4-CTA clusters leave SMs idle
-  // (fewer can be resident at once); one-CTA clusters measured faster.
-  (void)units_per_block;
-  return 1;
+std::atomic<int> g_tiling{0};   // moe_set_gemm_tiling
+
+// Resident CTA pairs of the pair-tiled kernel on the current device (cached per device).
+template <int EPI>
+int max_pairs() {
+  static std::mutex mu;
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return num_sms() / 2;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cached[dev] == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(num_sms() / 2 * 2), 1, 1);
+    cfg.blockDim = dim3(gk::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = gk::Layout<true>::SMEM_ALLOC;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, fp8_gemm_kernel<EPI, true>, &cfg) != cudaSuccess ||
+        n <= 0) {
+      cudaGetLastError();
+      n = num_sms() / 2;
+    }
+    cached[dev] = n;
+  }
+  return cached[dev];
 }
 
-template <int EPI>
+template <int EPI, bool PAIR>
 int launch_gemm_kernel(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p,
-                       int cs, long long max_units, cudaStream_t stream) {
-  constexpr int smem = gk::Layout<EPI>::SMEM_ALLOC;
-  auto kern = fp8_gemm_kernel<EPI>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-        cudaSuccess)
-      return MOE_ERR_CUDA;
-    attr_set = true;
+                       long long units, cudaStream_t stream) {
+  constexpr int smem = gk::Layout<PAIR>::SMEM_ALLOC;
+  auto kern = fp8_gemm_kernel<EPI, PAIR>;
+  if (set_max_dynamic_smem(reinterpret_cast<const void*>(kern), smem) != MOE_OK)
+    return MOE_ERR_CUDA;
+  if (!PAIR) {
+    long long grid = num_sms();                    // persistent: one CTA per SM
+    if (units < grid) grid = units;
+    if (grid < 1) grid = 1;
+    kern<<<static_cast<unsigned>(grid), gk::THREADS, smem, stream>>>(tmA, tmB, p);
+    return check_launch();
   }
+  long long pairs = max_pairs<EPI>();
+  if (units < pairs) pairs = units;
+  if (pairs < 1) pairs = 1;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
+  attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
   cfg.blockDim = dim3(gk::THREADS, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  // as many clusters as can be resident at once (the kernel is persistent)
-  static int max_clusters[5] = {0, 0, 0, 0, 0};
-  if (max_clusters[cs] == 0) {
-    cfg.gridDim = dim3(static_cast<unsigned>(num_sms() / cs * cs), 1, 1);
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) n = num_sms() / cs;
-    max_clusters[cs] = n;
-  }
-  long long clusters = max_clusters[cs];
-  if (max_units < clusters) clusters = max_units;
-  if (clusters < 1) clusters = 1;
-  cfg.gridDim = dim3(static_cast<unsigned>(clusters * cs), 1, 1);
   if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p) != cudaSuccess) return MOE_ERR_CUDA;
   return check_launch();
 }
 
+template <bool PAIR>
+int launch_tiling(const GemmArgs& a, GemmEpilogue epi, const GemmParams& p,
+                  cudaStream_t stream) {
+  using namespace gk;
+  using L = Layout<PAIR>;
+  CUtensorMap tmA, tmB;
+  if (!encode_tmap_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.A, a.K, a.M, a.K, BK, ROWS))
+    return MOE_ERR_CUDA;
+  if (!encode_tmap_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.B,
+                      a.K, static_cast<uint64_t>(a.G) * a.N, a.K, BK, L::B_ROWS))
+    return MOE_ERR_CUDA;
+  // an upper bound of the work units (each segment adds at most one partial M block)
+  const long long units = (static_cast<long long>(a.M) / L::BM + a.G) * ((a.N + BN - 1) / BN);
+  if (epi == kEpiSwiGLU) return launch_gemm_kernel<kEpiSwiGLU, PAIR>(tmA, tmB, p, units, stream);
+  return launch_gemm_kernel<kEpiBF16, PAIR>(tmA, tmB, p, units, stream);
+}
+
 }  // namespace
+
+void set_gemm_tiling(int mode) { g_tiling.store(mode); }
+int gemm_tiling() { return g_tiling.load(); }
 
 int launch_fp8_gemm(const GemmArgs& a, GemmEpilogue epi, cudaStream_t stream) {
   using namespace gk;
   if (a.M == 0) return MOE_OK;
   if (a.N % 128 != 0 || (epi == kEpiSwiGLU && a.N % BN != 0)) return MOE_ERR_UNSUPPORTED;
-  const int units = (a.N + BN - 1) / BN;                        // CTA units per row block
-  const int cs = pick_cluster(units);
-  CUtensorMap tmA, tmB;
-  if (!encode_tmap_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.A, a.K, a.M, a.K, BK, BM / cs))
-    return MOE_ERR_CUDA;
-  if (!encode_tmap_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.B,
-                      a.K, static_cast<uint64_t>(a.G) * a.N, a.K, BK, BN))
-    return MOE_ERR_CUDA;
   GemmParams p;
   p.sA = a.sA; p.sB = a.sB; p.seg = a.seg;
   p.G = a.G; p.M = a.M; p.N = a.N; p.K = a.K;
   p.C = a.C; p.ldc = a.ldc; p.hq = a.hq; p.sh = a.sh; p.status = a.status;
-  const long long max_units = (static_cast<long long>(a.M) / BM + a.G) * (units / cs);
-  if (epi == kEpiSwiGLU) return launch_gemm_kernel<kEpiSwiGLU>(tmA, tmB, p, cs, max_units, stream);
-  return launch_gemm_kernel<kEpiBF16>(tmA, tmB, p, cs, max_units, stream);
+  p.wait_ns = a.wait_ns ? a.wait_ns : kWaitLimitNs;
+  p.stall = a.stall;
+  // Automatic choice: the single tiling.  Measured on this B300, the pair tiling runs the
+  // same promotion per SM behind a longer release round trip (the buffer is free only when
+  // both CTAs' promotion warps have folded it in) and is about half as fast, dense or
+  // grouped; it stays selectable.
+  const int mode = g_tiling.load();
+  const bool pair = mode == 2;
+  return pair ? launch_tiling<true>(a, epi, p, stream) : launch_tiling<false>(a, epi, p, stream);
 }
 
 }  // namespace moe

@@ -142,20 +142,6 @@ MOE_DEV uint32_t ue8m0_word(float s, bool& bad) {
 
 MOE_DEV float silu_mx(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
-// The power-of-two scale rule of this variant: the smallest 2^k >= 2^-126 with
-// 448 * 2^k >= amax (448 = 1.75 * 2^8), exactly, from amax's exponent and mantissa.
-MOE_DEV float pow2_scale(float amax) {
-  if (amax == 0.0f) return 1.0f;
-  uint32_t b = __float_as_uint(amax);
-  int e = static_cast<int>((b >> 23) & 0xFFu) - 127;
-  if (((b >> 23) & 0xFFu) == 0) {
-    b = __float_as_uint(amax * 18446744073709551616.0f);   // * 2^64, exact
-    e = static_cast<int>((b >> 23) & 0xFFu) - 127 - 64;
-  }
-  const int k = max(e - 8 + ((b & 0x7FFFFFu) > 0x600000u ? 1 : 0), -126);
-  return __uint_as_float(static_cast<uint32_t>(k + 127) << 23);
-}
-
 template <int BM>
 MOE_DEV void decode_unit(int unit, const int* ustart, const int* seg, int G, int& g, int& m0,
                          int& rows_valid, int& nt) {
@@ -509,7 +495,7 @@ __global__ void __launch_bounds__(mx::THREADS, 1)
         ax[grp * BM + row] = amax;
         named_bar_sync_or(EPI_BAR, EPI_WARPS * 32, false);
         amax = fmaxf(amax, ax[(grp ^ 1) * BM + row]);
-        const float sc = pow2_scale(amax);
+        const float sc = pow2_scale_from_amax(amax);
         const float rs = __frcp_rn(sc);                     // exact: sc is a power of two
         const bool store = row < rv;
         const int f = p.N / 2;

@@ -15,6 +15,9 @@ int num_sms();
 // Raise a kernel's dynamic shared-memory limit on the current device (once per device).
 int set_max_dynamic_smem(const void* func, int bytes);
 
+// Unique ID of the current CUDA context (runtime.cu); false when none is current.
+bool current_context_id(unsigned long long* id);
+
 // MOE_OK if the last launch succeeded, else MOE_ERR_CUDA (and clears the error).
 int check_launch();
 
@@ -79,8 +82,14 @@ struct GemmArgs {
   uint8_t* hq;           // kEpiSwiGLU: [M][N/2] E4M3
   float* sh;             // kEpiSwiGLU: [N/256][M]
   int32_t* status;
+  uint64_t wait_ns;      // 0: the default limit of every mbarrier wait
+  int stall;             // failure-path test: the scheduler waits on a barrier nothing arrives on
 };
 int launch_fp8_gemm(const GemmArgs& a, GemmEpilogue epi, cudaStream_t stream);
+// CTA tiling of the grouped GEMM: 0 automatic, 1 one CTA per 128-row tile, 2 CTA pairs
+// per 256-row tile (tcgen05 cta_group::2).  Process-wide.
+void set_gemm_tiling(int mode);
+int gemm_tiling();
 
 // MX-native grouped GEMM (gemm_mx.cu): power-of-two block scales applied by the tensor
 // core.  A rows already in segment order.  kEpiBF16 writes C; kEpiSwiGLU writes hq / sh

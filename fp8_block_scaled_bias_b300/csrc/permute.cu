@@ -186,8 +186,10 @@ int launch_permute(const int32_t* idx, int T, int K, int E, int include_shared,
 // Scratch for moe_permute_noalloc: the per-chunk expert histograms live in this
 // file-scope device array instead of caller memory.  Every GPU that loads the library
 // holds it (1 MiB) until the process exits.  In host code the name is only a host-side
-// stand-in, so its device address is looked up with cudaGetSymbolAddress, once per
-// device, while that device is current.
+// stand-in, so its device address is looked up with cudaGetSymbolAddress while the
+// device is current: on the first call on each device, and again whenever that device's
+// CUDA context has changed since (cudaDeviceReset destroys the context that the address
+// belonged to; context IDs are never reused within a process).
 
 constexpr long long kNoAllocScratchInts = 262144;          // 1 MiB of int32
 static __device__ __align__(256) int32_t g_permute_scratch[kNoAllocScratchInts];
@@ -196,6 +198,7 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
 int32_t* g_scratch_ptr[kMaxDevices] = {nullptr};
+unsigned long long g_scratch_ctx[kMaxDevices] = {0};
 }  // namespace
 
 long long permute_noalloc_max_ints() { return kNoAllocScratchInts; }
@@ -204,13 +207,17 @@ int permute_noalloc_scratch(int32_t** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
+  unsigned long long ctx = 0;
+  const bool have_ctx = current_context_id(&ctx);
+  if (!g_scratch_ptr[dev] || !have_ctx || ctx != g_scratch_ctx[dev]) {
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_permute_scratch) != cudaSuccess || !ptr) {
       cudaGetLastError();
       return MOE_ERR_CUDA;
     }
     g_scratch_ptr[dev] = static_cast<int32_t*>(ptr);
+    // the lookup made the device's context current if none was
+    g_scratch_ctx[dev] = current_context_id(&ctx) ? ctx : 0;
   }
   *out = g_scratch_ptr[dev];
   return MOE_OK;

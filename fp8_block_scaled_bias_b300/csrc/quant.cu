@@ -11,22 +11,6 @@
 namespace moe {
 
 namespace {
-// Power-of-two scale rule (the MX-native variant): the smallest s = 2^k with 448 * s >= amax,
-// found exactly from amax's exponent and mantissa (448 = 1.75 * 2^8), at least 2^-126;
-// s = 1 for amax == 0.  Division by it is exact.
-MOE_DEV float pow2_scale_from_amax(float amax) {
-  if (amax == 0.0f) return 1.0f;
-  uint32_t b = __float_as_uint(amax);
-  int e = static_cast<int>((b >> 23) & 0xFFu) - 127;
-  if (((b >> 23) & 0xFFu) == 0) {                         // subnormal amax: rescale exactly
-    b = __float_as_uint(amax * 18446744073709551616.0f);  // * 2^64
-    e = static_cast<int>((b >> 23) & 0xFFu) - 127 - 64;
-  }
-  int k = e - 8 + ((b & 0x7FFFFFu) > 0x600000u ? 1 : 0);
-  k = max(k, -126);
-  return __uint_as_float(static_cast<uint32_t>(k + 127) << 23);
-}
-
 template <bool POW2>
 MOE_DEV float scale_rule(float amax) {
   return POW2 ? pow2_scale_from_amax(amax) : e4m3_scale_from_amax(amax);

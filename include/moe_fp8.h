@@ -138,7 +138,9 @@ size_t moe_permute_ws_bytes(int T, int K, int E);
  *     every GPU that loads the library holds it until the process exits.  Calls whose
  *     scratch need, ceil(T/128) * E int32, exceeds it return MOE_ERR_UNSUPPORTED.
  *   - The first call on each device looks up the array's device address (with that
- *     device current); make that first call before any stream capture.
+ *     device current); make that first call before any stream capture.  The lookup is
+ *     repeated when the device's CUDA context has changed (after cudaDeviceReset), so
+ *     make the first call after a reset before any capture too.
  *   - Every call shares the one array and nothing in it needs to start at zero (each
  *     call writes every entry it reads).  Calls that overlap on the GPU, e.g. on two
  *     streams without ordering between them, race on it: serialise them.
@@ -212,6 +214,29 @@ int fp8_blockscaled_grouped_gemm(const uint8_t* A, const float* sA, int M_a,
                                  uint16_t* C, int ldc, int32_t* dev_status,
                                  void* ws, size_t ws_bytes, void* stream);
 size_t fp8_grouped_gemm_ws_bytes(int M, int K, int has_a_rows);
+
+/* CTA tiling of fp8_blockscaled_grouped_gemm, moe_gate_up_fp8 and moe_swiglu_fp8_fwd
+ * (a performance choice; results are the same bits either way):
+ *   0  automatic (the default): tiling 1 (on B300 tiling 2 measured about half as fast);
+ *   1  one CTA per 128-row x 256-column tile (tcgen05 cta_group::1);
+ *   2  two CTAs of a cluster per 256-row x 256-column tile: one tcgen05 cta_group::2
+ *      MMA over both CTAs' shared memory, each CTA loading half of the weight tile.
+ * The setting is process-wide and applies to calls made after it.  Returns
+ * MOE_ERR_INVALID_ARG for any other mode. */
+int moe_set_gemm_tiling(int mode);
+int moe_get_gemm_tiling(void);
+
+/* Failure-path test of the kernels' bounded waits; not for production use.  Runs
+ * fp8_blockscaled_grouped_gemm (a_rows = NULL, same arguments) with every mbarrier wait
+ * limited to wait_ns nanoseconds (1e5 <= wait_ns <= 2e9) and the MMA scheduler first
+ * waiting on a barrier that nothing arrives on.  That wait expires: the kernel writes
+ * MOE_ERR_DEVICE_TIMEOUT to dev_status (required), stops issuing work, lets its copies
+ * and tensor-core operations in flight finish, frees its TMEM and returns, leaving C
+ * partly unwritten.  The GPU stays usable for the next call. */
+int moe_test_gemm_wait_expiry(const uint8_t* A, const float* sA, const uint8_t* B,
+                              const float* sB, const int32_t* seg_offsets, int G, int M, int N,
+                              int K, uint16_t* C, int ldc, int32_t* dev_status,
+                              unsigned long long wait_ns, void* stream);
 
 /* MX-native variant ([sum] core idea 6(a), core idea 8 "native group-scaled MMA"): the
  * same C as fp8_blockscaled_grouped_gemm (A rows in segment order, no a_rows) when every

@@ -1,6 +1,9 @@
 """GPU parity of the tcgen05 block-scaled grouped GEMM (through the C-ABI) against the
 oracle's exact definition: dense and grouped, ragged and empty segments, a half-width
-last N tile, gathered A rows, and the five full-size sweep shapes on sampled rows."""
+last N tile, gathered A rows, and the five full-size sweep shapes on sampled rows.  The
+small cases run under both CTA tilings (one CTA per 128-row tile; CTA pairs sharing one
+cta_group::2 MMA per 256-row tile).  The failure path of the bounded waits is exercised
+by a launch whose scheduler waits on a barrier nothing arrives on."""
 
 import numpy as np
 import pytest
@@ -13,6 +16,14 @@ from tolerance import assert_close, bf16_to_f32
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
+
+
+@pytest.fixture(params=[1, 2], ids=["single", "pair"])
+def tiling(request, lib):
+    L = lib.load()
+    assert L.moe_set_gemm_tiling(request.param) == 0
+    yield request.param
+    L.moe_set_gemm_tiling(0)
 
 
 def _codes(rows, cols, seed):
@@ -56,8 +67,8 @@ def _check(C, ref, what):
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 256, 128), (128, 256, 128), (200, 256, 512),
-                                   (300, 512, 1024), (129, 384, 256)])
-def test_dense_gemm(M, N, K):
+                                   (300, 512, 1024), (129, 384, 256), (513, 384, 640)])
+def test_dense_gemm(M, N, K, tiling):
     A, B = _codes(M, K, 1), _codes(N, K, 2)
     sA = workloads.gen_scales((K // 128, M), sub_seed=3)
     sB = workloads.gen_scales((1, N // 128, K // 128), sub_seed=4)
@@ -65,7 +76,7 @@ def test_dense_gemm(M, N, K):
     _check(C, _ref(A, sA, B[None], sB, [0, M]), f"dense {M}x{N}x{K}")
 
 
-def test_grouped_ragged_segments():
+def test_grouped_ragged_segments(tiling):
     counts = [0, 130, 1, 256, 77, 0, 128]
     seg = np.concatenate([[0], np.cumsum(counts)]).tolist()
     M, N, K, G = seg[-1], 384, 256, len(counts)
@@ -77,7 +88,7 @@ def test_grouped_ragged_segments():
     _check(C, _ref(A, sA, B, sB, seg), "grouped")
 
 
-def test_grouped_rows_past_last_segment_untouched():
+def test_grouped_rows_past_last_segment_untouched(tiling):
     seg = [0, 100, 100, 150]
     M, N, K = 300, 256, 128
     A = _codes(M, K, 9)
@@ -92,7 +103,7 @@ def test_grouped_rows_past_last_segment_untouched():
     _check(C[:150], _ref(A, sA, B, sB, seg), "prefix rows")
 
 
-def test_grouped_with_gathered_rows():
+def test_grouped_with_gathered_rows(tiling):
     T, K, N = 90, 256, 256
     rng = np.random.default_rng(0)
     a_rows = np.concatenate([rng.permutation(T)[:50], rng.permutation(T)[:70], np.arange(T)])
@@ -105,7 +116,7 @@ def test_grouped_with_gathered_rows():
     _check(C, _ref(A, sA, B, sB, seg, a_rows), "gathered")
 
 
-def test_bad_segment_table_is_reported():
+def test_bad_segment_table_is_reported(tiling):
     A = torch.zeros(64, 128, dtype=torch.uint8, device=DEV)
     sA = torch.ones(1, 64, device=DEV)
     B = torch.zeros(2, 256, 128, dtype=torch.uint8, device=DEV)
@@ -120,7 +131,7 @@ def test_bad_segment_table_is_reported():
     assert ops.status_value(st) == -6
 
 
-def test_closed_form_all_ones():
+def test_closed_form_all_ones(tiling):
     M, N, K = 256, 256, 1024
     A = torch.full((M, K), 0x38, dtype=torch.uint8)          # E4M3 1.0
     B = torch.full((1, N, K), 0x38, dtype=torch.uint8)
@@ -161,3 +172,68 @@ def test_sweep_recipe_normal_operands():
     exact = a.to(torch.bfloat16).double().numpy()[rows] @ b.double().numpy().T
     # FP8 quantisation error against the unquantised product: a few percent of RMS
     assert np.abs(C[rows] - exact).mean() / np.sqrt((exact ** 2).mean()) < 0.05
+
+
+def test_grouped_many_ragged_segments_both_tilings_equal(lib):
+    """40 segments of 0..300 rows (empty ones, 1-row ones, ends on and off the 128- and
+    256-row grids), N with a half-filled last tile: both tilings give the oracle's result
+    and the same bits."""
+    rng = np.random.default_rng(17)
+    counts = rng.integers(0, 300, 40)
+    counts[[3, 9, 20]] = 0
+    counts[[5, 6]] = 1
+    counts[[11, 12]] = [128, 256]
+    seg = np.concatenate([[0], np.cumsum(counts)]).tolist()
+    M, N, K, G = seg[-1], 640, 384, len(counts)
+    A = _codes(M, K, 41)
+    sA = workloads.gen_scales((K // 128, M), sub_seed=42)
+    B = _codes(G * N, K, 43).view(G, N, K)
+    sB = workloads.gen_scales((G, N // 128, K // 128), sub_seed=44)
+    L = lib.load()
+    outs = []
+    try:
+        for mode in (1, 2):
+            L.moe_set_gemm_tiling(mode)
+            outs.append(_run(A, sA, B, sB, seg, M))
+    finally:
+        L.moe_set_gemm_tiling(0)
+    assert np.array_equal(outs[0], outs[1])
+    _check(outs[1], _ref(A, sA, B, sB, seg), "40 ragged segments")
+
+
+@pytest.mark.parametrize("mode", [1, 2], ids=["single", "pair"])
+def test_bounded_wait_expiry_reports_and_recovers(lib, mode):
+    """Failure detection without a GPU fault: the scheduler waits on a barrier nothing
+    arrives on, with every wait limited to 1 ms.  The kernel must report
+    MOE_ERR_DEVICE_TIMEOUT, drain, free its TMEM and return within milliseconds, and the
+    next (normal) launch on the same GPU must be correct."""
+    import time
+    from fp8_block_scaled_bias_b300._lib import call
+    L = lib.load()
+    M, N, K = 512, 512, 1024
+    A = torch.full((M, K), 0x38, dtype=torch.uint8, device=DEV)     # E4M3 1.0
+    B = torch.full((2, N, K), 0x38, dtype=torch.uint8, device=DEV)
+    sA = torch.ones(K // 128, M, device=DEV)
+    sB = torch.ones(2, N // 128, K // 128, device=DEV)
+    seg = torch.tensor([0, 200, M], dtype=torch.int32, device=DEV)
+    C = torch.zeros(M, N, dtype=torch.bfloat16, device=DEV)
+    try:
+        L.moe_set_gemm_tiling(mode)
+        st = ops.new_status(DEV)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        call("moe_test_gemm_wait_expiry", A.data_ptr(), sA.data_ptr(), B.data_ptr(),
+             sB.data_ptr(), seg.data_ptr(), 2, M, N, K, C.data_ptr(), N, st.data_ptr(),
+             1_000_000, torch.cuda.current_stream().cuda_stream)
+        torch.cuda.synchronize()
+        dt = time.perf_counter() - t0
+        assert ops.status_value(st) == -4                 # MOE_ERR_DEVICE_TIMEOUT
+        assert dt < 1.0, dt
+        # the same GEMM without the stall: the context is healthy and the result exact
+        st = ops.new_status(DEV)
+        ops.grouped_gemm(A, sA, B, sB, seg, M, status=st, out=C)
+        torch.cuda.synchronize()
+        assert ops.status_value(st) == 0
+        assert (bf16_to_f32(C) == K).all()
+    finally:
+        L.moe_set_gemm_tiling(0)

@@ -80,6 +80,25 @@ def test_grouped_ragged_mx_gemm():
     assert_close(C, _ref(A, sA, B, sB, seg), what="mx grouped")
 
 
+@pytest.mark.parametrize("N", [384, 1152])
+def test_grouped_ragged_mx_gemm_paired_tile(N):
+    """M >= 256 * G selects the paired 256-row tile (two 128-row accumulators sharing each
+    224-column B tile).  Empty segments, lengths off the 128- and 256-row grids, and N not
+    a multiple of 224, so 224-column tiles straddle the 128-column weight-scale blocks
+    and the last tile is partly filled."""
+    counts = [0, 905, 1, 257, 0, 383, 511, 1]
+    seg = np.concatenate([[0], np.cumsum(counts)]).tolist()
+    G, K = len(counts), 384
+    M = seg[-1]
+    assert M >= 256 * G
+    A = workloads.gen_fp8_codes(M, K, sub_seed=61)
+    B = torch.stack([workloads.gen_fp8_codes(N, K, sub_seed=70 + g) for g in range(G)])
+    sA = _pow2_scales((K // 128, M), 62)
+    sB = _pow2_scales((G, N // 128, K // 128), 63)
+    C = _run(A, sA, B, sB, seg, M)
+    assert_close(C, _ref(A, sA, B, sB, seg), what=f"mx grouped paired N={N}")
+
+
 def test_pow2_quantisers_bit_exact():
     x = workloads.gen_x(workloads.V3)[:512]
     q, s = ops.quant_1x128(x.to(DEV), pow2=True)
