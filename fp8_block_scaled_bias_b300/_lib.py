@@ -38,6 +38,15 @@ SIGNATURES = {
     "fp8_blockscaled_grouped_gemm": (_I, [_P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P, _I,
                                           _P, _P, _SZ, _P]),
     "fp8_grouped_gemm_ws_bytes": (_SZ, [_I, _I, _I]),
+    "moe_gate_up_fp8_train": (_I, [_P, _P, _P, _I, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
+    "fp8_transpose_128x128": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P]),
+    "moe_padded_rows_cap": (_I, [_I, _I]),
+    "moe_segment_pad_offsets": (_I, [_P, _I, _P, _P, _P]),
+    "moe_combine_bwd_rows": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
+    "fp8_quant_128x1_pow2": (_I, [_P, _I, _P, _I, _P, _P, _I, _I, _P, _P, _P, _P]),
+    "moe_swiglu_bwd_fp8": (_I, [_P, _P, _P, _I, _I, _P, _P, _I, _I, _P, _P, _P, _P, _P, _P,
+                                _P]),
+    "fp8_wgrad_grouped_gemm": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P]),
     "moe_set_gemm_tiling": (_I, [_I]),
     "moe_get_gemm_tiling": (_I, []),
     "moe_test_gemm_wait_expiry": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _I, _P,

@@ -364,6 +364,109 @@ int moe_gate_up_mx(const uint8_t* xq_rows, const float* sx_rows, const int32_t* 
                              nullptr, 0, hq, sh, moe::kEpiSwiGLU, dev_status, as_stream(stream));
 }
 
+// ---- backward of the experts (training) ----------------------------------------------
+
+int moe_gate_up_fp8_train(const uint8_t* xq_rows, const float* sx_rows, const int32_t* offsets,
+                          int rows, const uint8_t* w13, const float* s13, int n_segments, int d,
+                          int f, uint8_t* hq, float* sh, uint8_t* guq, float* sgu,
+                          int32_t* dev_status, void* stream) {
+  if (rows < 0 || d <= 0 || f <= 0 || d % 128 != 0 || f % 128 != 0 || n_segments < 1)
+    return MOE_ERR_INVALID_ARG;
+  const int st = check_gemm_dims(n_segments, rows, 2 * f, d);
+  if (st != MOE_OK) return st;
+  if (rows == 0) return MOE_OK;
+  if (!xq_rows || !sx_rows || !offsets || !w13 || !s13 || !hq || !sh || !guq || !sgu)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(xq_rows) || !aligned16(w13) || !aligned16(hq) || !aligned16(guq))
+    return MOE_ERR_INVALID_ARG;
+  GemmArgs up{};
+  up.A = xq_rows; up.sA = sx_rows; up.B = w13; up.sB = s13; up.seg = offsets;
+  up.G = n_segments; up.M = rows; up.N = 2 * f; up.K = d;
+  up.hq = hq; up.sh = sh; up.guq = guq; up.sgu = sgu; up.status = dev_status;
+  return moe::launch_fp8_gemm(up, moe::kEpiSwiGLUCache, as_stream(stream));
+}
+
+int fp8_transpose_128x128(const uint8_t* w, const float* s, int G, int rows, int cols,
+                          int gate_up_interleaved, uint8_t* wT, float* sT, void* stream) {
+  if (G < 1 || rows < 0 || cols < 0 || rows % 128 != 0 || cols % 128 != 0)
+    return MOE_ERR_INVALID_ARG;
+  if (gate_up_interleaved && rows % 256 != 0) return MOE_ERR_INVALID_ARG;
+  if (static_cast<long long>(G) > 65535) return MOE_ERR_UNSUPPORTED;
+  if (rows == 0 || cols == 0) return MOE_OK;
+  if (!w || !s || !wT || !sT) return MOE_ERR_INVALID_ARG;
+  return moe::launch_transpose_fp8(w, s, G, rows, cols, gate_up_interleaved != 0, wT, sT,
+                                   as_stream(stream));
+}
+
+int moe_padded_rows_cap(int rows, int G) {
+  if (rows < 0 || G < 1) return -1;
+  const long long cap = (static_cast<long long>(rows) + 127LL * G + 127) / 128 * 128;
+  return cap > INT32_MAX ? -1 : static_cast<int>(cap);
+}
+
+int moe_segment_pad_offsets(const int32_t* offsets, int G, int32_t* pad, int32_t* dev_status,
+                            void* stream) {
+  if (G < 1) return MOE_ERR_INVALID_ARG;
+  if (G > 1024) return MOE_ERR_UNSUPPORTED;
+  if (!offsets || !pad) return MOE_ERR_INVALID_ARG;
+  return moe::launch_seg_pad(offsets, G, pad, dev_status, as_stream(stream));
+}
+
+int moe_combine_bwd_rows(const uint16_t* dy, const float* topk_gate, const int32_t* row_of,
+                         int T, int K, int d, int shared_row_base, int n_rows, uint16_t* dy_rows,
+                         int32_t* dev_status, void* stream) {
+  if (T < 0 || K < 1 || d <= 0 || d % 8 != 0 || n_rows < 0) return MOE_ERR_INVALID_ARG;
+  if (K > 32) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!dy || !topk_gate || !row_of || !dy_rows || !aligned16(dy) || !aligned16(dy_rows))
+    return MOE_ERR_INVALID_ARG;
+  return moe::launch_dispatch_grad(dy, topk_gate, row_of, T, K, d, shared_row_base, n_rows,
+                                   dy_rows, dev_status, as_stream(stream));
+}
+
+int fp8_quant_128x1_pow2(const uint16_t* src, int src_rows, const int32_t* rows, int cols,
+                         const int32_t* offsets, const int32_t* pad, int G, int kcap,
+                         uint8_t* qT, float* sT, int32_t* dev_status, void* stream) {
+  if (src_rows < 0 || cols <= 0 || cols % 128 != 0 || G < 1 || kcap < 0 || kcap % 128 != 0)
+    return MOE_ERR_INVALID_ARG;
+  if (G > 1024 || cols / 128 > 65535) return MOE_ERR_UNSUPPORTED;
+  if (kcap == 0) return MOE_OK;
+  if (!src || !offsets || !pad || !qT || !sT || !aligned16(src) || !aligned16(qT))
+    return MOE_ERR_INVALID_ARG;
+  return moe::launch_regroup_128x1(src, src_rows, rows, cols, offsets, pad, G, kcap / 128, kcap,
+                                   qT, sT, dev_status, as_stream(stream));
+}
+
+int moe_swiglu_bwd_fp8(const uint8_t* guq, const float* sgu, const uint16_t* dh, int rows, int f,
+                       const int32_t* offsets, const int32_t* pad, int G, int kcap,
+                       uint8_t* dguq, float* sdgu, uint8_t* hT, float* shT, uint8_t* dguT,
+                       float* sdguT, void* stream) {
+  if (rows < 0 || f <= 0 || f % 128 != 0 || G < 1 || kcap < 0 || kcap % 128 != 0)
+    return MOE_ERR_INVALID_ARG;
+  if (G > 1024 || f / 128 > 65535) return MOE_ERR_UNSUPPORTED;
+  if (rows == 0 || kcap == 0) return MOE_OK;
+  if (!guq || !sgu || !dh || !offsets || !pad || !dguq || !sdgu || !hT || !shT || !dguT || !sdguT)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(guq) || !aligned16(dh) || !aligned16(hT) || !aligned16(dguT))
+    return MOE_ERR_INVALID_ARG;
+  return moe::launch_swiglu_bwd(guq, sgu, dh, rows, f, offsets, pad, G, kcap / 128, kcap, dguq,
+                                sdgu, hT, shT, dguT, sdguT, as_stream(stream));
+}
+
+int fp8_wgrad_grouped_gemm(const uint8_t* aT, const float* saT, const uint8_t* bT,
+                           const float* sbT, const int32_t* pad, int G, int I, int J, int kcap,
+                           float* dW, int32_t* dev_status, void* stream) {
+  if (G < 1 || I <= 0 || J <= 0 || kcap <= 0 || I % 128 != 0 || J % 128 != 0 || kcap % 128 != 0)
+    return MOE_ERR_INVALID_ARG;
+  if (G > 1024 || static_cast<long long>(G) * (I / 128) * ((J + 255) / 256) > INT32_MAX)
+    return MOE_ERR_UNSUPPORTED;
+  if (!aT || !saT || !bT || !sbT || !pad || !dW || !aligned16(aT) || !aligned16(bT) ||
+      !aligned16(dW))
+    return MOE_ERR_INVALID_ARG;
+  return moe::launch_wgrad_gemm(aT, saT, bT, sbT, pad, G, I, J, kcap, dW, dev_status,
+                                as_stream(stream));
+}
+
 // ---- combine, bias update, workspace -------------------------------------------------
 
 int moe_combine(const uint16_t* y_rows, int n_rows, const int32_t* row_of, const float* gate,

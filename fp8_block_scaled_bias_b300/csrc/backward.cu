@@ -85,9 +85,17 @@ __global__ void __launch_bounds__(1024) seg_pad_kernel(const int32_t* __restrict
 
 // ---- weight transpose (setup) ------------------------------------------------------------
 
-// One 64 x 64 byte tile per block: dst[g][c][r] = src[g][r][c].
+// Row r of the gate-first matrix [gate; up] in the 64-row interleaved layout.
+MOE_DEV int interleaved_row(int r, int R) {
+  const int half = R / 2;
+  return r < half ? (r / 64) * 128 + (r % 64) : ((r - half) / 64) * 128 + 64 + (r - half) % 64;
+}
+
+// One 64 x 64 byte tile per block: dst[g][c][r] = src[g][row(r)][c], row(r) = r, or the
+// interleaved position of gate-first row r.
 __global__ void __launch_bounds__(256) transpose_kernel(const uint8_t* __restrict__ src, int R,
-                                                        int C, uint8_t* __restrict__ dst) {
+                                                        int C, int interleaved,
+                                                        uint8_t* __restrict__ dst) {
   __shared__ uint8_t tile[64][65];
   const long long g = blockIdx.z;
   const int r0 = blockIdx.y * 64, c0 = blockIdx.x * 64;
@@ -95,7 +103,8 @@ __global__ void __launch_bounds__(256) transpose_kernel(const uint8_t* __restric
   uint8_t* d = dst + g * R * static_cast<long long>(C);
   for (int i = threadIdx.x; i < 64 * 64; i += 256) {
     const int rr = i >> 6, cc = i & 63;
-    tile[rr][cc] = s[static_cast<long long>(r0 + rr) * C + c0 + cc];
+    const int sr = interleaved ? interleaved_row(r0 + rr, R) : r0 + rr;
+    tile[rr][cc] = s[static_cast<long long>(sr) * C + c0 + cc];
   }
   __syncthreads();
   for (int i = threadIdx.x; i < 64 * 64; i += 256) {
@@ -104,15 +113,18 @@ __global__ void __launch_bounds__(256) transpose_kernel(const uint8_t* __restric
   }
 }
 
+// sT[g][cb][rb] = s[g][blk(rb)][cb]; with the interleaved source the block scales alternate
+// gate block i (2i), up block i (2i + 1), so gate-first block rb is 2 rb, or 2 (rb - RB/2) + 1.
 __global__ void transpose_scales_kernel(const float* __restrict__ s, int RB, int CB, int G,
-                                        float* __restrict__ sT) {
+                                        int interleaved, float* __restrict__ sT) {
   const long long n = static_cast<long long>(G) * RB * CB;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
     const long long g = i / (RB * CB);
     const int rem = static_cast<int>(i % (RB * CB));
     const int rb = rem / CB, cb = rem % CB;
-    sT[(g * CB + cb) * RB + rb] = s[i];
+    const int sb = interleaved ? (rb < RB / 2 ? 2 * rb : 2 * (rb - RB / 2) + 1) : rb;
+    sT[(g * CB + cb) * RB + rb] = s[(g * RB + sb) * CB + cb];
   }
 }
 
@@ -247,9 +259,12 @@ __global__ void __launch_bounds__(kBwdThreads) swiglu_bwd_kernel(
     const int32_t* __restrict__ pad, int G, int ldq, uint8_t* __restrict__ dguq,
     float* __restrict__ sdgu, uint8_t* __restrict__ hT, float* __restrict__ shT,
     uint8_t* __restrict__ dguT, float* __restrict__ sdguT) {
-  __shared__ __align__(16) uint8_t tg[kTile][kTile + 16];
-  __shared__ __align__(16) uint8_t tu[kTile][kTile + 16];
-  __shared__ __align__(16) uint16_t tdh[kTile][kTile + 8];
+  // dynamic shared memory: the tile's g codes, u codes (rows padded to 144 bytes) and dh
+  // (rows padded to 136 BF16 values), 71,680 bytes
+  extern __shared__ __align__(16) uint8_t bwd_smem[];
+  auto tg = reinterpret_cast<uint8_t(*)[kTile + 16]>(bwd_smem);
+  auto tu = reinterpret_cast<uint8_t(*)[kTile + 16]>(bwd_smem + kTile * (kTile + 16));
+  auto tdh = reinterpret_cast<uint16_t(*)[kTile + 8]>(bwd_smem + 2 * kTile * (kTile + 16));
   __shared__ float sg_s[kTile], su_s[kTile];
   __shared__ float rmax_g[kTile], rmax_u[kTile];
   __shared__ float cpart[3][2][kTile];
@@ -318,7 +333,7 @@ __global__ void __launch_bounds__(kBwdThreads) swiglu_bwd_kernel(
   uint32_t wh[16], wg[16], wu[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) { wh[i] = 0; wg[i] = 0; wu[i] = 0; }
-#pragma unroll 4
+#pragma unroll
   for (int j = 0; j < 64; ++j) {
     const int r = half * 64 + j;
     const SwigluVals v = swiglu_bwd_at(tg[r][c], tu[r][c], sg_s[r], su_s[r],
@@ -363,14 +378,16 @@ int launch_seg_pad(const int32_t* seg, int G, int32_t* pad, int32_t* status, cud
   return check_launch();
 }
 
-int launch_transpose_fp8(const uint8_t* src, const float* s, int G, int R, int C, uint8_t* dst,
-                         float* sT, cudaStream_t stream) {
-  transpose_kernel<<<dim3(C / 64, R / 64, G), 256, 0, stream>>>(src, R, C, dst);
+int launch_transpose_fp8(const uint8_t* src, const float* s, int G, int R, int C, bool interleaved,
+                         uint8_t* dst, float* sT, cudaStream_t stream) {
+  transpose_kernel<<<dim3(C / 64, R / 64, G), 256, 0, stream>>>(src, R, C, interleaved ? 1 : 0,
+                                                                dst);
   int st = check_launch();
   if (st != MOE_OK) return st;
   const long long n = static_cast<long long>(G) * (R / 128) * (C / 128);
   const int blocks = static_cast<int>(min(4096LL, (n + 255) / 256));
-  transpose_scales_kernel<<<blocks, 256, 0, stream>>>(s, R / 128, C / 128, G, sT);
+  transpose_scales_kernel<<<blocks, 256, 0, stream>>>(s, R / 128, C / 128, G,
+                                                      interleaved ? 1 : 0, sT);
   return check_launch();
 }
 
@@ -399,7 +416,10 @@ int launch_swiglu_bwd(const uint8_t* guq, const float* sgu, const uint16_t* dh, 
                       const int32_t* seg, const int32_t* pad, int G, int max_blocks, int ldq,
                       uint8_t* dguq, float* sdgu, uint8_t* hT, float* shT, uint8_t* dguT,
                       float* sdguT, cudaStream_t stream) {
-  swiglu_bwd_kernel<<<dim3(max_blocks, f / kTile), kBwdThreads, 0, stream>>>(
+  constexpr int smem = 2 * kTile * (kTile + 16) + kTile * (kTile + 8) * 2;
+  if (set_max_dynamic_smem(reinterpret_cast<const void*>(swiglu_bwd_kernel), smem) != MOE_OK)
+    return MOE_ERR_CUDA;
+  swiglu_bwd_kernel<<<dim3(max_blocks, f / kTile), kBwdThreads, smem, stream>>>(
       guq, sgu, dh, R, f, seg, pad, G, ldq, dguq, sdgu, hT, shT, dguT, sdguT);
   return check_launch();
 }

@@ -96,9 +96,10 @@ struct Layout {
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;   // tmem slot, abort, total, bad
   static constexpr int OFF_SEG = OFF_MISC + 16;
   static constexpr int OFF_TSTART = OFF_SEG + (MAX_G + 1) * 4;
-  static constexpr int OFF_AMAX = OFF_TSTART + (MAX_G + 1) * 4;   // [2 bufs][2 groups][128]
+  // row max-abs exchange: [2 bufs][h, gate, up][2 column halves][128 rows]
+  static constexpr int OFF_AMAX = OFF_TSTART + (MAX_G + 1) * 4;
   // per-thread rings of prefetched scales: sA [SPF][EPI_THREADS], sB [SPF][EPI_WARPS][2]
-  static constexpr int OFF_SCALE_A = OFF_AMAX + 2 * 2 * ROWS * 4;
+  static constexpr int OFF_SCALE_A = OFF_AMAX + 2 * 3 * 2 * ROWS * 4;
   static constexpr int OFF_SCALE_B = OFF_SCALE_A + SPF * EPI_THREADS * 4;
   static constexpr int SMEM_USED = OFF_SCALE_B + SPF * EPI_WARPS * 2 * 4;
   static constexpr int SMEM_ALLOC = SMEM_USED + 1024;              // 1024-B alignment slack
@@ -115,6 +116,8 @@ struct GemmParams {
   int ldc;
   uint8_t* hq;
   float* sh;
+  uint8_t* guq;          // training forward: g, u cached as E4M3 [M][N] (gate cols first)
+  float* sgu;            // and their 1x128 scales [N/128][M]
   int32_t* status;
   uint64_t wait_ns;      // limit of every mbarrier wait
   int stall;             // != 0: the scheduler waits on a barrier nothing arrives on
@@ -160,6 +163,13 @@ MOE_DEV void mbar_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
 MOE_DEV uint32_t e4m3x4(float a, float b, float c, float d, float rs) {
   const uint32_t lo = f32x2_to_e4m3x2(__fmul_rn(a, rs), __fmul_rn(b, rs));
   const uint32_t hi = f32x2_to_e4m3x2(__fmul_rn(c, rs), __fmul_rn(d, rs));
+  return lo | (hi << 16);
+}
+
+// The activation quantiser's rule exactly: q = E4M3(fl32(x / s)), correctly rounded division.
+MOE_DEV uint32_t e4m3x4_div(const float* x, float s) {
+  const uint32_t lo = f32x2_to_e4m3x2(__fdiv_rn(x[0], s), __fdiv_rn(x[1], s));
+  const uint32_t hi = f32x2_to_e4m3x2(__fdiv_rn(x[2], s), __fdiv_rn(x[3], s));
   return lo | (hi << 16);
 }
 
@@ -221,6 +231,9 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
   using namespace gk;
   using L = Layout<PAIR>;
   constexpr int STAGES = L::STAGES, BM = L::BM;
+  // SwiGLU epilogue; CACHE: also keep its inputs g, u in FP8 (training forward)
+  constexpr bool SWIGLU = EPI == kEpiSwiGLU || EPI == kEpiSwiGLUCache;
+  constexpr bool CACHE = EPI == kEpiSwiGLUCache;
   extern __shared__ uint8_t gemm_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(gemm_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -444,7 +457,7 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
     // TMEM columns of this thread's eight 16-column chunks, from its half's first column
     // (SwiGLU: 4 gate then 4 up)
     auto col_of = [](int c) {
-      return static_cast<uint32_t>((EPI == kEpiSwiGLU) ? (c < 4 ? 0 : 64) + (c & 3) * 16 : c * 16);
+      return static_cast<uint32_t>((SWIGLU) ? (c < 4 ? 0 : 64) + (c & 3) * 16 : c * 16);
     };
     // Scale prefetch: every K block needs sA[kb][row] (this thread's row) and the one or
     // two weight scales of the tile's N blocks.  They are copied into shared-memory rings
@@ -463,8 +476,8 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
       // issue the copies of the cursor's K block into ring slot pf_it % SPF, then advance
       if (pf_live) {
         // (a half-filled last tile has no second N block: read a valid scale, unused)
-        const int nb0 = (EPI == kEpiSwiGLU) ? 2 * pf_nt : min(2 * pf_nt + grp, NB - 1);
-        const int nb1 = (EPI == kEpiSwiGLU) ? 2 * pf_nt + 1 : nb0;
+        const int nb0 = (SWIGLU) ? 2 * pf_nt : min(2 * pf_nt + grp, NB - 1);
+        const int nb1 = (SWIGLU) ? 2 * pf_nt + 1 : nb0;
         const int slot = static_cast<int>(pf_it % SPF);
         const int arow = min(pf_m0 + row_off + row, p.M - 1);
         cp_async_4(ring_a + slot * EPI_THREADS * 4,
@@ -491,9 +504,9 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
     float nsa = ring_a_f[0], nsb0 = ring_b_f[0], nsb1 = ring_b_f[1];
 
     uint32_t it = 0;
-    int ucount = 0;
+    uint32_t xch = 0;                                    // row max-abs exchanges so far
     bool ok = true;
-    for (int unit = first_unit; ok && unit < total; unit += unit_stride, ++ucount) {
+    for (int unit = first_unit; ok && unit < total; unit += unit_stride) {
       int g, m0, nt;
       decode_unit<BM>(unit, ustart, seg, G, g, m0, nt);
       const int r0 = m0 + row_off;                       // first row of this CTA's part
@@ -564,6 +577,51 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
           }
         }
       } else {
+        const int f = p.N / 2;
+        // The two threads of a row (column halves grp 0 and 1) exchange row max-abs values
+        // through shared memory; exchange xch uses buffer xch & 1.
+        auto exchange = [&](float v0, float v1, float& m0, float& m1) {
+          float* ax = amax_x + (xch & 1) * 3 * 2 * ROWS;  // [value][half][row]
+          ax[grp * ROWS + row] = v0;
+          ax[(2 + grp) * ROWS + row] = v1;
+          mbar_arrive(amax_bar(xch & 1));
+          const bool okx =
+              mbar_wait_warp(amax_bar(xch & 1), (xch >> 1) & 1, abort_flag, p.status, wait_ns);
+          m0 = fmaxf(v0, ax[(grp ^ 1) * ROWS + row]);
+          m1 = fmaxf(v1, ax[(2 + (grp ^ 1)) * ROWS + row]);
+          ++xch;
+          return okx;
+        };
+        if (CACHE) {
+          // training forward: the SwiGLU inputs g, u (gate and up columns of this row) are
+          // kept in FP8 for the backward, one 1x128 scale per 128 hidden columns
+          float ag = 0.0f, au = 0.0f;
+#pragma unroll
+          for (int i = 0; i < 64; ++i) {
+            ag = fmaxf(ag, fabsf(acc[i]));
+            au = fmaxf(au, fabsf(acc[64 + i]));
+          }
+          if (!exchange(ag, au, ag, au)) { ok = false; break; }
+          const float sg = e4m3_scale_from_amax(ag), su = e4m3_scale_from_amax(au);
+          if (row < rv) {
+            uint8_t* gr = p.guq + static_cast<long long>(r0 + row) * p.N + nt * 128 + grp * 64;
+            uint4* gd = reinterpret_cast<uint4*>(gr);
+            uint4* ud = reinterpret_cast<uint4*>(gr + f);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float* gv = acc + 16 * j;
+              const float* uv = acc + 64 + 16 * j;
+              gd[j] = make_uint4(e4m3x4_div(gv, sg), e4m3x4_div(gv + 4, sg),
+                                 e4m3x4_div(gv + 8, sg), e4m3x4_div(gv + 12, sg));
+              ud[j] = make_uint4(e4m3x4_div(uv, su), e4m3x4_div(uv + 4, su),
+                                 e4m3x4_div(uv + 8, su), e4m3x4_div(uv + 12, su));
+            }
+            if (grp == 0) {
+              p.sgu[static_cast<long long>(nt) * p.M + r0 + row] = sg;
+              p.sgu[static_cast<long long>(f / 128 + nt) * p.M + r0 + row] = su;
+            }
+          }
+        }
         // h = silu(gate) * up for this thread's 64 hidden columns
         float amax = 0.0f;
 #pragma unroll
@@ -571,18 +629,11 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
           acc[i] = __fmul_rn(silu_f32(acc[i]), acc[64 + i]);
           amax = fmaxf(amax, fabsf(acc[i]));
         }
-        const int buf = ucount & 1;
-        amax_x[(buf * 2 + grp) * ROWS + row] = amax;
-        mbar_arrive(amax_bar(buf));
-        if (!mbar_wait_warp(amax_bar(buf), (ucount >> 1) & 1, abort_flag, p.status, wait_ns)) {
-          ok = false;
-          break;
-        }
-        amax = fmaxf(amax, amax_x[(buf * 2 + (grp ^ 1)) * ROWS + row]);
+        float unused;
+        if (!exchange(amax, 0.0f, amax, unused)) { ok = false; break; }
         const float s = e4m3_scale_from_amax(amax);
         const float rs = __frcp_rn(s);
         if (row < rv) {
-          const int f = p.N / 2;
           uint4* dst = reinterpret_cast<uint4*>(p.hq + static_cast<long long>(r0 + row) * f +
                                                 nt * 128 + grp * 64);
 #pragma unroll
@@ -697,6 +748,8 @@ int launch_tiling(const GemmArgs& a, GemmEpilogue epi, const GemmParams& p,
   // an upper bound of the work units (each segment adds at most one partial M block)
   const long long units = (static_cast<long long>(a.M) / L::BM + a.G) * ((a.N + BN - 1) / BN);
   if (epi == kEpiSwiGLU) return launch_gemm_kernel<kEpiSwiGLU, PAIR>(tmA, tmB, p, units, stream);
+  if (epi == kEpiSwiGLUCache)
+    return launch_gemm_kernel<kEpiSwiGLUCache, PAIR>(tmA, tmB, p, units, stream);
   return launch_gemm_kernel<kEpiBF16, PAIR>(tmA, tmB, p, units, stream);
 }
 
@@ -708,11 +761,13 @@ int gemm_tiling() { return g_tiling.load(); }
 int launch_fp8_gemm(const GemmArgs& a, GemmEpilogue epi, cudaStream_t stream) {
   using namespace gk;
   if (a.M == 0) return MOE_OK;
-  if (a.N % 128 != 0 || (epi == kEpiSwiGLU && a.N % BN != 0)) return MOE_ERR_UNSUPPORTED;
+  if (a.N % 128 != 0 || (epi != kEpiBF16 && a.N % BN != 0)) return MOE_ERR_UNSUPPORTED;
+  if (epi == kEpiSwiGLUCache && (!a.guq || !a.sgu)) return MOE_ERR_INVALID_ARG;
   GemmParams p;
   p.sA = a.sA; p.sB = a.sB; p.seg = a.seg;
   p.G = a.G; p.M = a.M; p.N = a.N; p.K = a.K;
   p.C = a.C; p.ldc = a.ldc; p.hq = a.hq; p.sh = a.sh; p.status = a.status;
+  p.guq = a.guq; p.sgu = a.sgu;
   p.wait_ns = a.wait_ns ? a.wait_ns : kWaitLimitNs;
   p.stall = a.stall;
   // Automatic choice: the single tiling.  Measured on this B300, the pair tiling runs the

@@ -26,6 +26,15 @@
 // TMEM: columns [0, 256) accumulator; scale slot j at 256 + 16 j: 4 columns of row scales
 // (word (lane l, column c) = rows l % 32 + 32 c, the byte repeated for the four 32-deep
 // steps), then 8 columns of column scales laid out the same way for 256 B rows.
+//
+// kEpiF32 is the Wgrad of the expert backward ("DeepSeek-V3" book, ch. 17 "One linear layer
+// creates three GEMMs"; ch. 16 "Why transposition is not trivial"): the contraction runs
+// over token rows, so both operands arrive transposed, K-major over each expert's rows
+// padded to 128-row blocks, with one power-of-two scale per (row block, output row) and
+// per (row block, output column) -- the 128x1 regrouping.  A unit is (expert, 128-row
+// tile, 256-column tile) and its K loop covers that expert's row blocks only; an expert
+// without rows gets zeros.  The block scales of B vary per column, which the tensor
+// core's per-column scale factors take directly.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -99,6 +108,7 @@ struct MxParams {
   int ldc;
   uint8_t* hq;           // SwiGLU epilogue: [M][N/2] E4M3
   float* sh;             // SwiGLU epilogue: [N/256][M] power-of-two scales
+  float* Cf;             // F32 epilogue (Wgrad): [G][M][ldc]
   int32_t* status;
 };
 
@@ -182,6 +192,7 @@ __global__ void __launch_bounds__(mx::THREADS, 1)
   constexpr int OFF_WSUM = TL::OFF_WSUM, OFF_AMAX = TL::OFF_AMAX;
   constexpr uint32_t SF_COL0 = TL::SF_COL0, SFB_OFF = TL::SFB_OFF, SFA1_OFF = TL::SFA1_OFF;
   static_assert(!PAIR || EPI == kEpiBF16, "the paired tile has the BF16 epilogue only");
+  constexpr bool WG = EPI == kEpiF32;        // Wgrad: per-expert K ranges, column scales
   extern __shared__ uint8_t mx_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(mx_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -208,12 +219,21 @@ __global__ void __launch_bounds__(mx::THREADS, 1)
   const int NT = (p.N + BN - 1) / BN;        // N tiles (the last may be half-filled)
   const int NB = p.N / 128;                  // weight-scale rows per segment
   const int KB = p.K / BK;
+  const int MT = p.M / 128;                  // Wgrad: row tiles per expert
 
   // ---- segment table and unit prefix ----
   if (tid == 0) { *abort_flag = 0; *bad = 0; }
   for (int i = tid; i <= G; i += THREADS) seg[i] = p.seg[i];
   __syncthreads();
-  {
+  if (WG) {
+    // padded row offsets: start at 0, non-decreasing, whole 128-row blocks, within K
+    for (int g = tid; g < G; g += THREADS)
+      if (seg[g + 1] < seg[g] || (seg[g + 1] & (BK - 1)) != 0) *bad = 1;
+    if (tid == 0) {
+      if (seg[0] != 0 || seg[G] > p.K) *bad = 1;
+      *total_units = G * MT * NT;
+    }
+  } else {
     const int per = (G + THREADS - 1) / THREADS;
     const int g0 = min(G, tid * per), g1 = min(G, g0 + per);
     int local = 0;
@@ -251,6 +271,22 @@ __global__ void __launch_bounds__(mx::THREADS, 1)
     return;
   }
   const int total = *total_units;
+  // unit -> (segment g, first row m0, valid rows rv, N tile nt, first K block kb0, K blocks)
+  auto unit_info = [&](int unit, int& g, int& m0, int& rv, int& nt, int& kb0, int& nkb) {
+    if (WG) {
+      g = unit / (MT * NT);
+      const int r = unit - g * MT * NT;
+      nt = r / MT;
+      m0 = (r - nt * MT) * 128;
+      rv = 128;
+      kb0 = seg[g] / BK;
+      nkb = (seg[g + 1] - seg[g]) / BK;
+    } else {
+      decode_unit<BM>(unit, ustart, seg, G, g, m0, rv, nt);
+      kb0 = 0;
+      nkb = KB;
+    }
+  };
 
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) { mbar_init(full_bar(s), 1); mbar_init(empty_bar(s), 1); }
@@ -278,16 +314,16 @@ __global__ void __launch_bounds__(mx::THREADS, 1)
       uint32_t it = 0;
       bool ok = true;
       for (int unit = first_unit; ok && unit < total; unit += unit_stride) {
-        int g, m0, rv, nt;
-        decode_unit<BM>(unit, ustart, seg, G, g, m0, rv, nt);
-        const int brow = g * p.N + nt * BN;
-        for (int kb = 0; kb < KB; ++kb, ++it) {
+        int g, m0, rv, nt, kb0, nkb;
+        unit_info(unit, g, m0, rv, nt, kb0, nkb);
+        const int brow = (WG ? 0 : g * p.N) + nt * BN;
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
           if (!mbar_wait(empty_bar(s), ph ^ 1, abort_flag, p.status)) { ok = false; break; }
           mbar_arrive_expect_tx(full_bar(s), STAGE_BYTES);
-          tma_load_2d(sbase + OFF_A + s * A_BYTES, &tmA, kb * BK, m0, full_bar(s));
-          tma_load_2d(sbase + OFF_B + s * B_BYTES, &tmB, kb * BK, brow, full_bar(s));
+          tma_load_2d(sbase + OFF_A + s * A_BYTES, &tmA, (kb0 + kb) * BK, m0, full_bar(s));
+          tma_load_2d(sbase + OFF_B + s * B_BYTES, &tmB, (kb0 + kb) * BK, brow, full_bar(s));
         }
       }
       if (!ok) {
@@ -300,7 +336,12 @@ __global__ void __launch_bounds__(mx::THREADS, 1)
     uint32_t it = 0;
     bool ok = true;
     for (int unit = first_unit; ok && unit < total; unit += unit_stride) {
-      for (int kb = 0; kb < KB; ++kb, ++it) {
+      int nkb = KB;
+      if (WG) {                      // once per tile: the expert's K range
+        int g, m0, rv, nt, kb0;
+        unit_info(unit, g, m0, rv, nt, kb0, nkb);
+      }
+      for (int kb = 0; kb < nkb; ++kb, ++it) {
         if (named_bar_sync_or(MMA_BAR, 64, false)) { ok = false; break; }
         if (lane == 0) {
           const int s = it % STAGES;
@@ -320,7 +361,7 @@ __global__ void __launch_bounds__(mx::THREADS, 1)
           }
           mma_commit(empty_bar(s));
           mma_commit(sf_empty_bar(j));
-          if (kb == KB - 1) mma_commit(tfull_bar);
+          if (kb == nkb - 1) mma_commit(tfull_bar);
         }
         __syncwarp();
       }
@@ -334,8 +375,14 @@ __global__ void __launch_bounds__(mx::THREADS, 1)
     // ---------------- MMA scheduler ----------------
     uint32_t it = 0, tt = 0;
     bool ok = true;
-    for (int unit = first_unit; ok && unit < total; unit += unit_stride, ++tt) {
-      for (int kb = 0; kb < KB; ++kb, ++it) {
+    for (int unit = first_unit; ok && unit < total; unit += unit_stride) {
+      int nkb = KB;
+      if (WG) {
+        int g, m0, rv, nt, kb0;
+        unit_info(unit, g, m0, rv, nt, kb0, nkb);
+        if (nkb == 0) continue;      // no accumulator use: the epilogue writes zeros
+      }
+      for (int kb = 0; kb < nkb; ++kb, ++it) {
         int good = 1;
         if (lane == 0) {
           const int s = it % STAGES;
@@ -348,6 +395,7 @@ __global__ void __launch_bounds__(mx::THREADS, 1)
         tc_fence_before();
         if (named_bar_sync_or(MMA_BAR, 64, good == 0)) { ok = false; break; }
       }
+      ++tt;
     }
   } else if (warp >= SF_WARP0 && warp < SF_WARP0 + SF_WARPS) {
     // ---------------- scale writers ----------------
@@ -355,12 +403,13 @@ __global__ void __launch_bounds__(mx::THREADS, 1)
     uint32_t it = 0;
     bool ok = true, badscale = false;
     for (int unit = first_unit; ok && unit < total; unit += unit_stride) {
-      int g, m0, rv, nt;
-      decode_unit<BM>(unit, ustart, seg, G, g, m0, rv, nt);
+      int g, m0, rv, nt, kb0, nkb;
+      unit_info(unit, g, m0, rv, nt, kb0, nkb);
       const int nb0 = 2 * nt, nb1 = min(2 * nt + 1, NB - 1);
       const int n0 = nt * BN;
-      const float* sbg = p.sB + static_cast<long long>(g) * NB * KB;
-      for (int kb = 0; kb < KB; ++kb, ++it) {
+      const float* sbg = p.sB + (WG ? 0LL : static_cast<long long>(g) * NB * KB);
+      for (int kb = 0; kb < nkb; ++kb, ++it) {
+        const int kbg = kb0 + kb;                   // K block in the scale arrays
         const int j = it % SF_SLOTS;
         if (!mbar_wait_warp(sf_empty_bar(j), ((it / SF_SLOTS) & 1) ^ 1, abort_flag, p.status)) {
           ok = false;
@@ -371,14 +420,21 @@ __global__ void __launch_bounds__(mx::THREADS, 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const int r = min(m0 + lane + 32 * c, p.M - 1);
-          wa[c] = ue8m0_word(__ldg(p.sA + static_cast<long long>(kb) * p.M + r), badscale);
+          wa[c] = ue8m0_word(__ldg(p.sA + static_cast<long long>(kbg) * p.M + r), badscale);
           if (PAIR) {
             const int r1 = min(m0 + 128 + lane + 32 * c, p.M - 1);
-            wa1[c] = ue8m0_word(__ldg(p.sA + static_cast<long long>(kb) * p.M + r1), badscale);
+            wa1[c] = ue8m0_word(__ldg(p.sA + static_cast<long long>(kbg) * p.M + r1), badscale);
           }
         }
         // B row n of the tile is row 32 c + lane of column c.
-        if (PAIR) {
+        if (WG) {
+          // one scale per column (output column n0 + n) of this row block
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const int n = min(n0 + 32 * c + lane, p.N - 1);
+            wb[c] = ue8m0_word(__ldg(p.sB + static_cast<long long>(kbg) * p.N + n), badscale);
+          }
+        } else if (PAIR) {
           // 224-row tiles: a row's weight block is (n0 + n) / 128 (rows past N: any block)
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
@@ -414,15 +470,46 @@ __global__ void __launch_bounds__(mx::THREADS, 1)
     const int row = q * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
     uint32_t tt = 0;
-    for (int unit = first_unit; unit < total; unit += unit_stride, ++tt) {
-      int g, m0, rv, nt;
-      decode_unit<BM>(unit, ustart, seg, G, g, m0, rv, nt);
+    for (int unit = first_unit; unit < total; unit += unit_stride) {
+      int g, m0, rv, nt, kb0, nkb;
+      unit_info(unit, g, m0, rv, nt, kb0, nkb);
+      if (WG && nkb == 0) {
+        // an expert without rows: its weight gradient is zero (no accumulator use)
+        if (nt * BN + grp * 128 < p.N) {
+          float4* dst = reinterpret_cast<float4*>(
+              p.Cf + (static_cast<long long>(g) * p.M + m0 + row) * p.ldc + nt * BN + grp * 128);
+#pragma unroll 8
+          for (int i = 0; i < 32; ++i) dst[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        }
+        continue;
+      }
       const bool good = mbar_wait_warp(tfull_bar, tt & 1, abort_flag, p.status);
       // all eight warps agree before any of them uses the barrier below
       if (named_bar_sync_or(EPI_BAR, EPI_WARPS * 32, !good)) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + lane_addr + static_cast<uint32_t>(grp * 128);
-      if (PAIR) {
+      if (WG) {
+        // FP32 weight gradient rows: this thread's row, 128 columns of its half
+        const bool store = nt * BN + grp * 128 < p.N;
+        float4* dst = reinterpret_cast<float4*>(
+            p.Cf + (static_cast<long long>(g) * p.M + m0 + row) * p.ldc + nt * BN + grp * 128);
+#pragma unroll
+        for (int c = 0; c < 8; c += 2) {
+          uint32_t v[2][16];
+          tmem_ld_32x32b_x16(tbase + c * 16, v[0]);
+          tmem_ld_32x32b_x16(tbase + c * 16 + 16, v[1]);
+          tmem_ld_wait();
+          if (store) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                dst[(c + h) * 4 + i] =
+                    make_float4(__uint_as_float(v[h][4 * i]), __uint_as_float(v[h][4 * i + 1]),
+                                __uint_as_float(v[h][4 * i + 2]), __uint_as_float(v[h][4 * i + 3]));
+          }
+        }
+      } else if (PAIR) {
         // sub-tile grp (rows 128 grp + row of the block), all BN columns of its accumulator
         const int trow = grp * 128 + row;
         const uint32_t abase = tmem_base + lane_addr + static_cast<uint32_t>(grp * BN);
@@ -525,6 +612,7 @@ __global__ void __launch_bounds__(mx::THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty_bar);
+      ++tt;
     }
   }
 
@@ -546,17 +634,20 @@ namespace {
 template <int EPI, bool PAIR>
 int launch_mx_kernel(const uint8_t* A, const uint8_t* B, const MxParams& p, cudaStream_t stream) {
   using TL = mx::Tile<PAIR>;
+  constexpr bool WG = EPI == kEpiF32;
   CUtensorMap tmA, tmB;
+  // Wgrad: A = a^T [M][K] and B = b^T [N][K] shared by every expert; else B is [G][N][K]
   if (!encode_tmap_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, p.K, p.M, p.K, mx::BK, TL::BM))
     return MOE_ERR_CUDA;
   if (!encode_tmap_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, p.K,
-                      static_cast<uint64_t>(p.G) * p.N, p.K, mx::BK, TL::BN))
+                      static_cast<uint64_t>(WG ? 1 : p.G) * p.N, p.K, mx::BK, TL::BN))
     return MOE_ERR_CUDA;
   if (set_max_dynamic_smem(reinterpret_cast<const void*>(fp8_mx_gemm_kernel<EPI, PAIR>),
                            TL::SMEM_ALLOC) != MOE_OK)
     return MOE_ERR_CUDA;
   const long long units =
-      (static_cast<long long>(p.M) / TL::BM + p.G) * ((p.N + TL::BN - 1) / TL::BN);
+      WG ? static_cast<long long>(p.G) * (p.M / 128) * ((p.N + TL::BN - 1) / TL::BN)
+         : (static_cast<long long>(p.M) / TL::BM + p.G) * ((p.N + TL::BN - 1) / TL::BN);
   long long grid = num_sms();
   if (units < grid) grid = units;
   if (grid < 1) grid = 1;
@@ -575,7 +666,7 @@ int launch_mx_gemm(const uint8_t* A, const float* sA, const uint8_t* B, const fl
   MxParams p;
   p.sA = sA; p.sB = sB; p.seg = seg;
   p.G = G; p.M = M; p.N = N; p.K = K;
-  p.C = C; p.ldc = ldc; p.hq = hq; p.sh = sh; p.status = status;
+  p.C = C; p.ldc = ldc; p.hq = hq; p.sh = sh; p.Cf = nullptr; p.status = status;
   // SwiGLU: the 256-column gate/up tile.  BF16 output: two 128-row sub-tiles per CTA share
   // each B tile when segments average at least 256 rows; shorter segments would leave the
   // second sub-tile mostly empty, so they keep the single tile (measured: V3's routed
@@ -585,6 +676,17 @@ int launch_mx_gemm(const uint8_t* A, const float* sA, const uint8_t* B, const fl
   if (static_cast<long long>(M) >= 256LL * G)
     return launch_mx_kernel<kEpiBF16, true>(A, B, p, stream);
   return launch_mx_kernel<kEpiBF16, false>(A, B, p, stream);
+}
+
+int launch_wgrad_gemm(const uint8_t* aT, const float* sA, const uint8_t* bT, const float* sB,
+                      const int32_t* pad, int G, int I, int J, int Kcap, float* C,
+                      int32_t* status, cudaStream_t stream) {
+  if (I % 128 != 0 || J % 128 != 0 || Kcap % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  MxParams p;
+  p.sA = sA; p.sB = sB; p.seg = pad;
+  p.G = G; p.M = I; p.N = J; p.K = Kcap;
+  p.C = nullptr; p.ldc = J; p.hq = nullptr; p.sh = nullptr; p.Cf = C; p.status = status;
+  return launch_mx_kernel<kEpiF32, false>(aT, bT, p, stream);
 }
 
 }  // namespace moe

@@ -69,7 +69,7 @@ int launch_gather_rows_fp8(const uint8_t* src, const float* src_scale, int src_r
                            cudaStream_t stream);
 
 // Grouped block-scaled GEMM (tcgen05).  Epilogue kinds:
-enum GemmEpilogue { kEpiBF16 = 0, kEpiSwiGLU = 1 };
+enum GemmEpilogue { kEpiBF16 = 0, kEpiSwiGLU = 1, kEpiF32 = 2, kEpiSwiGLUCache = 3 };
 struct GemmArgs {
   const uint8_t* A;      // [M][K] rows already in segment order
   const float* sA;       // [K/128][M]
@@ -81,6 +81,8 @@ struct GemmArgs {
   int ldc;
   uint8_t* hq;           // kEpiSwiGLU: [M][N/2] E4M3
   float* sh;             // kEpiSwiGLU: [N/256][M]
+  uint8_t* guq;          // kEpiSwiGLU, training: g | u as E4M3 [M][N] (NULL: not cached)
+  float* sgu;            // and their 1x128 scales [N/128][M]
   int32_t* status;
   uint64_t wait_ns;      // 0: the default limit of every mbarrier wait
   int stall;             // failure-path test: the scheduler waits on a barrier nothing arrives on
@@ -98,6 +100,31 @@ int launch_mx_gemm(const uint8_t* A, const float* sA, const uint8_t* B, const fl
                    const int32_t* seg, int G, int M, int N, int K, uint16_t* C, int ldc,
                    uint8_t* hq, float* sh, GemmEpilogue epi, int32_t* status,
                    cudaStream_t stream);
+
+// Expert backward helpers (backward.cu).
+int launch_seg_pad(const int32_t* seg, int G, int32_t* pad, int32_t* status, cudaStream_t stream);
+// interleaved: src is the gate/up matrix with gate and up rows alternating in 64-row blocks
+// (and scales alternating gate block, up block); dst columns come out gate first, then up.
+int launch_transpose_fp8(const uint8_t* src, const float* s, int G, int R, int C, bool interleaved,
+                         uint8_t* dst, float* sT, cudaStream_t stream);
+int launch_dispatch_grad(const uint16_t* dy, const float* gate, const int32_t* row_of, int T,
+                         int K, int d, int shared_row_base, int n_rows, uint16_t* dy_rows,
+                         int32_t* status, cudaStream_t stream);
+int launch_regroup_128x1(const uint16_t* src, int src_rows, const int32_t* rows, int C,
+                         const int32_t* seg, const int32_t* pad, int G, int max_blocks, int ldq,
+                         uint8_t* qT, float* sT, int32_t* status, cudaStream_t stream);
+int launch_swiglu_bwd(const uint8_t* guq, const float* sgu, const uint16_t* dh, int R, int f,
+                      const int32_t* seg, const int32_t* pad, int G, int max_blocks, int ldq,
+                      uint8_t* dguq, float* sdgu, uint8_t* hT, float* shT, uint8_t* dguT,
+                      float* sdguT, cudaStream_t stream);
+
+// Wgrad of the expert backward (gemm_mx.cu): per expert e, C[e] [I][J] (FP32, row pitch J)
+// = sum over e's 128-row blocks rb of sA[rb][i] * sB[rb][j] * sum_p aT[i][p] * bT[j][p], with
+// aT [I][Kcap], bT [J][Kcap] FP8 (K-major over padded rows), power-of-two scales
+// [Kcap/128][I] and [Kcap/128][J], and pad [G+1] the experts' padded row offsets (device).
+int launch_wgrad_gemm(const uint8_t* aT, const float* sA, const uint8_t* bT, const float* sB,
+                      const int32_t* pad, int G, int I, int J, int Kcap, float* C,
+                      int32_t* status, cudaStream_t stream);
 
 int launch_router_logits(const uint16_t* x, int T, int d, const uint16_t* w_hilo, int E,
                          float* z, int32_t* status, void* ws, cudaStream_t stream);

@@ -15,6 +15,12 @@ tile holds matching gate and up columns.
 ``mx=True`` runs the MX-native variant: power-of-two scales for x, the weights and h,
 applied by the tensor core (tcgen05 kind::mxf8f6f4) instead of by software promotion;
 its weights come from ``make_weights(..., pow2=True)``.
+
+``train=True`` makes ``forward`` keep the SwiGLU inputs in FP8 and enables ``backward``:
+the experts' input and weight gradients from the three FP8 GEMMs of each linear layer
+("DeepSeek-V3" book, ch. 17 "One linear layer creates three GEMMs", "SwiGLU
+recomputation"; ch. 16 "Why transposition is not trivial").  The router and gate
+gradients are not computed.
 """
 
 from dataclasses import dataclass
@@ -84,10 +90,13 @@ def make_weights(cfg, device="cuda", base_seed=0, expert_fn=None, pow2=False):
 class MoELayer:
     """Buffers and the sequence of library calls for one layer forward."""
 
-    def __init__(self, cfg, weights, T=None, mx=False):
+    def __init__(self, cfg, weights, T=None, mx=False, train=False):
         self.cfg = cfg
         self.w = weights
         self.mx = mx
+        self.train = train
+        if train and mx:
+            raise ValueError("the training path uses the FP32-scale recipe")
         self.T = cfg.T if T is None else T
         T, E, K, d, f = self.T, cfg.E, cfg.K, cfg.d, cfg.f
         dev = weights.w13.device
@@ -108,6 +117,12 @@ class MoELayer:
         self.y = emp(T, d, dt=torch.bfloat16)
         self.status = ops.new_status(dev)
         self.seg_end = self.offsets[cfg.E + 1:cfg.E + 2]     # device int32: rows in use
+        if train:
+            self.guq = emp(self.rows, 2 * f, dt=torch.uint8)     # SwiGLU inputs, FP8
+            self.sgu = emp(2 * f // 128, self.rows)
+            self.x = None
+            self._wT = None
+            self._ones = torch.ones(T, K, dtype=torch.float32, device=dev)
 
     # kernel launches of one forward, by stage (bias_update adds one more)
     STAGE_LAUNCHES = {"router_logits": 1, "route": 1, "permute": 3, "quant_dispatch": 1,
@@ -135,8 +150,13 @@ class MoELayer:
         ops.quant_scatter_1x128(x, self.row_of, self.rows, self.T * cfg.K, self.status,
                                 out=(self.xq_rows, self.sx_rows), pow2=self.mx)
         mark("quant_dispatch")
-        ops.gate_up(self.xq_rows, self.sx_rows, self.offsets, w.w13, w.s13, self.status,
-                    out=(self.hq, self.sh), mx=self.mx)
+        if self.train:
+            ops.gate_up_train(self.xq_rows, self.sx_rows, self.offsets, w.w13, w.s13,
+                              self.status, out=(self.hq, self.sh, self.guq, self.sgu))
+            self.x = x
+        else:
+            ops.gate_up(self.xq_rows, self.sx_rows, self.offsets, w.w13, w.s13, self.status,
+                        out=(self.hq, self.sh), mx=self.mx)
         mark("gate_up")
         down = ops.mx_grouped_gemm if self.mx else ops.grouped_gemm
         down(self.hq, self.sh, w.w2, w.s2, self.offsets, self.rows, status=self.status,
@@ -147,6 +167,54 @@ class MoELayer:
         if residual:
             return self.y + x
         return self.y
+
+    # kernel launches of one backward
+    BACKWARD_LAUNCHES = 11
+
+    def transposed_weights(self):
+        """The Dgrad operands, made once: W2^T [E+1, f, d] and [W1; W3]^T [E+1, d, 2f] with
+        their 128x128 block scales transposed."""
+        if self._wT is None:
+            w = self.w
+            w2T, s2T = ops.transpose_128x128(w.w2, w.s2)
+            w13T, s13T = ops.transpose_128x128(w.w13, w.s13, gate_up_interleaved=True)
+            self._wT = (w2T, s2T, w13T, s13T)
+        return self._wT
+
+    def backward(self, dy, mark=None):
+        """dy BF16 [T, d] (gradient of the layer output) -> dict of dx BF16 [T, d] (through
+        the experts, not the router), dw13 FP32 [E+1, 2f, d] ([dW1; dW3], gate rows first)
+        and dw2 FP32 [E+1, d, f], plus the intermediate tensors.  Needs a forward with
+        train=True on the same layer first."""
+        if not self.train or self.x is None:
+            raise RuntimeError("backward needs a forward of a layer built with train=True")
+        cfg, T, K, E = self.cfg, self.T, self.cfg.K, self.cfg.E
+        rows, G = self.rows, E + 1
+        mark = mark or (lambda name: None)
+        w2T, s2T, w13T, s13T = self.transposed_weights()
+        st = self.status
+        dy_rows = ops.combine_bwd_rows(dy, self.gate, self.row_of, T * K, rows, status=st)
+        dyq, sdy = ops.quant_1x128(dy_rows)
+        dh = ops.grouped_gemm(dyq, sdy, w2T, s2T, self.offsets, rows, status=st)
+        mark("down_dgrad")
+        kcap = ops.padded_rows_cap(rows, G)
+        pad = ops.segment_pad_offsets(self.offsets, G, status=st)
+        dguq, sdgu, hT, shT, dguT, sdguT = ops.swiglu_bwd(self.guq, self.sgu, dh, self.offsets,
+                                                          pad, kcap)
+        mark("swiglu_bwd")
+        dx_rows = ops.grouped_gemm(dguq, sdgu, w13T, s13T, self.offsets, rows, status=st)
+        dx = ops.combine(dx_rows, self.row_of, self._ones, T * K, st)   # gates of 1
+        mark("gate_up_dgrad")
+        dyT, sdyT = ops.quant_128x1_pow2(dy_rows, self.offsets, pad, kcap, status=st)
+        dw2 = ops.wgrad(dyT, sdyT, hT, shT, pad, status=st)
+        mark("down_wgrad")
+        xT, sxT = ops.quant_128x1_pow2(self.x, self.offsets, pad, kcap, rows=self.row_token,
+                                       status=st)
+        dw13 = ops.wgrad(dguT, sdguT, xT, sxT, pad, status=st)
+        mark("gate_up_wgrad")
+        return dict(dx=dx, dw13=dw13, dw2=dw2, dy_rows=dy_rows, dh=dh, dx_rows=dx_rows,
+                    pad=pad, kcap=kcap, dguq=dguq, sdgu=sdgu, hT=hT, shT=shT, dguT=dguT,
+                    sdguT=sdguT, dyT=dyT, sdyT=sdyT, xT=xT, sxT=sxT)
 
     def bias_update(self, gamma):
         """Aux-loss-free bias step from this forward's expert loads (in place)."""

@@ -316,3 +316,131 @@ def combine(y_rows, row_of, gate, shared_row_base, status=None, out=None):
     call("moe_combine", _ptr(y_rows), y_rows.shape[0], _ptr(row_of), _ptr(gate), T, K, d,
          int(shared_row_base), _ptr(y), _ptr(status), _stream())
     return y
+
+
+# ---- backward of the experts (training) -------------------------------------------------
+
+def gate_up_train(xq_rows, sx_rows, offsets, w13, s13, status=None, out=None):
+    """Training-forward gate/up: (hq, sh) as gate_up, plus the SwiGLU inputs cached in FP8:
+    guq uint8 [rows, 2f] (gate columns first) with 1x128 scales sgu [2f/128, rows]."""
+    for t, dt, n in ((xq_rows, _U8, "xq_rows"), (sx_rows, _F32, "sx_rows"),
+                     (offsets, _I32, "offsets"), (w13, _U8, "w13"), (s13, _F32, "s13")):
+        _check(t, dt, n)
+    rows, d = xq_rows.shape
+    S, f2, _ = w13.shape
+    f = f2 // 2
+    dev = xq_rows.device
+    if out is None:
+        hq = torch.empty(rows, f, dtype=_U8, device=dev)
+        sh = torch.empty(f // 128, rows, dtype=_F32, device=dev)
+        guq = torch.empty(rows, 2 * f, dtype=_U8, device=dev)
+        sgu = torch.empty(2 * f // 128, rows, dtype=_F32, device=dev)
+    else:
+        hq, sh, guq, sgu = out
+    call("moe_gate_up_fp8_train", _ptr(xq_rows), _ptr(sx_rows), _ptr(offsets), rows, _ptr(w13),
+         _ptr(s13), S, d, f, _ptr(hq), _ptr(sh), _ptr(guq), _ptr(sgu), _ptr(status), _stream())
+    return hq, sh, guq, sgu
+
+
+def transpose_128x128(w, s, gate_up_interleaved=False):
+    """Transposed FP8 weights with transposed 128x128 block scales: w uint8 [G, R, C], s FP32
+    [G, R/128, C/128] -> (wT [G, C, R], sT [G, C/128, R/128]); gate_up_interleaved: w is the
+    64-row interleaved gate/up matrix and wT's columns come out gate first."""
+    _check(w, _U8, "w", 3)
+    _check(s, _F32, "s", 3)
+    G, R, C = w.shape
+    wT = torch.empty(G, C, R, dtype=_U8, device=w.device)
+    sT = torch.empty(G, C // 128, R // 128, dtype=_F32, device=w.device)
+    call("fp8_transpose_128x128", _ptr(w), _ptr(s), G, R, C, int(bool(gate_up_interleaved)),
+         _ptr(wT), _ptr(sT), _stream())
+    return wT, sT
+
+
+def padded_rows_cap(rows, G):
+    """Columns to allocate for the 128x1 (padded) layout of `rows` rows in G segments."""
+    cap = load().moe_padded_rows_cap(int(rows), int(G))
+    if cap < 0:
+        raise ValueError("bad rows / G")
+    return cap
+
+
+def segment_pad_offsets(offsets, G, status=None, out=None):
+    """int32 [G+1]: every segment's first padded row (128-row blocks per segment)."""
+    _check(offsets, _I32, "offsets", 1)
+    pad = out if out is not None else torch.empty(G + 1, dtype=_I32, device=offsets.device)
+    call("moe_segment_pad_offsets", _ptr(offsets), G, _ptr(pad), _ptr(status), _stream())
+    return pad
+
+
+def combine_bwd_rows(dy, gate, row_of, shared_row_base, n_rows, status=None, out=None):
+    """BF16 [n_rows, d] gradient of the expert output rows: gate * dy per routed row, dy
+    per shared row."""
+    _check(dy, _BF16, "dy", 2)
+    _check(gate, _F32, "gate", 2)
+    _check(row_of, _I32, "row_of", 2)
+    T, d = dy.shape
+    K = row_of.shape[1]
+    dy_rows = out if out is not None else torch.empty(n_rows, d, dtype=_BF16, device=dy.device)
+    call("moe_combine_bwd_rows", _ptr(dy), _ptr(gate), _ptr(row_of), T, K, d,
+         int(shared_row_base), n_rows, _ptr(dy_rows), _ptr(status), _stream())
+    return dy_rows
+
+
+def quant_128x1_pow2(src, offsets, pad, kcap, rows=None, status=None, out=None):
+    """128x1 power-of-two tiles of the segment-order rows (src[rows[r]] when gathering),
+    transposed: (qT uint8 [cols, kcap], sT FP32 [kcap/128, cols])."""
+    _check(src, _BF16, "src", 2)
+    _check(offsets, _I32, "offsets", 1)
+    _check(pad, _I32, "pad", 1)
+    if rows is not None:
+        _check(rows, _I32, "rows", 1)
+    cols = src.shape[1]
+    G = offsets.numel() - 1
+    if out is None:
+        qT = torch.empty(cols, kcap, dtype=_U8, device=src.device)
+        sT = torch.empty(kcap // 128, cols, dtype=_F32, device=src.device)
+    else:
+        qT, sT = out
+    call("fp8_quant_128x1_pow2", _ptr(src), src.shape[0], _ptr(rows), cols, _ptr(offsets),
+         _ptr(pad), G, kcap, _ptr(qT), _ptr(sT), _ptr(status), _stream())
+    return qT, sT
+
+
+def swiglu_bwd(guq, sgu, dh, offsets, pad, kcap, out=None):
+    """SwiGLU backward with recomputation: (dguq, sdgu, hT, shT, dguT, sdguT), see
+    include/moe_fp8.h."""
+    _check(guq, _U8, "guq", 2)
+    _check(sgu, _F32, "sgu", 2)
+    _check(dh, _BF16, "dh", 2)
+    rows, f = dh.shape
+    G = offsets.numel() - 1
+    dev = dh.device
+    if out is None:
+        out = (torch.empty(rows, 2 * f, dtype=_U8, device=dev),
+               torch.empty(2 * f // 128, rows, dtype=_F32, device=dev),
+               torch.empty(f, kcap, dtype=_U8, device=dev),
+               torch.empty(kcap // 128, f, dtype=_F32, device=dev),
+               torch.empty(2 * f, kcap, dtype=_U8, device=dev),
+               torch.empty(kcap // 128, 2 * f, dtype=_F32, device=dev))
+    dguq, sdgu, hT, shT, dguT, sdguT = out
+    call("moe_swiglu_bwd_fp8", _ptr(guq), _ptr(sgu), _ptr(dh), rows, f, _ptr(offsets),
+         _ptr(pad), G, kcap, _ptr(dguq), _ptr(sdgu), _ptr(hT), _ptr(shT), _ptr(dguT),
+         _ptr(sdguT), _stream())
+    return out
+
+
+def wgrad(aT, saT, bT, sbT, pad, status=None, out=None):
+    """FP32 dW [G, I, J] = per expert, sum over its 128-row blocks of the block-scaled
+    aT . bT^T (128x1 power-of-two scales applied by the tensor core)."""
+    _check(aT, _U8, "aT", 2)
+    _check(bT, _U8, "bT", 2)
+    _check(saT, _F32, "saT", 2)
+    _check(sbT, _F32, "sbT", 2)
+    _check(pad, _I32, "pad", 1)
+    I, kcap = aT.shape
+    J = bT.shape[0]
+    G = pad.numel() - 1
+    dW = out if out is not None else torch.empty(G, I, J, dtype=_F32, device=aT.device)
+    call("fp8_wgrad_grouped_gemm", _ptr(aT), _ptr(saT), _ptr(bT), _ptr(sbT), _ptr(pad), G, I, J,
+         kcap, _ptr(dW), _ptr(status), _stream())
+    return dW

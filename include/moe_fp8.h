@@ -305,6 +305,105 @@ int moe_gate_up_fp8(const uint8_t* xq_rows, const float* sx_rows, const int32_t*
                     int rows, const uint8_t* w13, const float* s13, int n_segments, int d,
                     int f, uint8_t* hq, float* sh, int32_t* dev_status, void* stream);
 
+/* ---- backward of the experts (training) -------------------------------------------- */
+
+/* The three GEMMs of a linear layer in training -- Fprop, Dgrad (input gradient,
+ * dX = dY W^T) and Wgrad (weight gradient, dW = X^T dY) -- all take FP8 inputs ([book]
+ * ch. 17 "One linear layer creates three GEMMs"; [sum] core idea 6).  Activation
+ * gradients keep 1x128 tiles ([book] ch. 17 "Backward grouping and gradient
+ * sensitivity").  Wgrad contracts over token rows, so its operands are regrouped into
+ * 128x1 tiles with power-of-two scales ([book] ch. 16 "Why transposition is not
+ * trivial"; ch. 17 "Attention-related saved activations"), and the MoE caches the
+ * SwiGLU inputs in FP8 and recomputes the SwiGLU output in backward ([book] ch. 17
+ * "SwiGLU recomputation").  One expert backward, rows in segment order:
+ *   moe_combine_bwd_rows    dY rows from dy and the gates
+ *   fp8_quant_1x128         dY -> 1x128 tiles
+ *   fp8_blockscaled_grouped_gemm(dYq, W2^T)           dh (BF16), down Dgrad
+ *   moe_swiglu_bwd_fp8      h recomputed from the cache; dG, dU; [dG|dU] 1x128 for the
+ *                           gate/up Dgrad; h^T and [dG|dU]^T 128x1 for the Wgrads
+ *   fp8_blockscaled_grouped_gemm([dG|dU]q, [W1;W3]^T) dX rows (BF16), gate/up Dgrad
+ *   moe_combine(dX rows, gates = 1)                   dx per token
+ *   fp8_quant_128x1_pow2    dY^T and the input rows X^T in 128x1 tiles
+ *   fp8_wgrad_grouped_gemm(dY^T, h^T) -> dW2;  (... [dG|dU]^T, X^T) -> [dW1; dW3]
+ * Padded row layout of the 128x1 tensors: every segment's rows are cut into 128-row
+ * blocks starting at its first row; block b of segment e sits at columns
+ * [pad[e] + 128 b, pad[e] + 128 b + 128) of a [C][kcap] matrix (pad from
+ * moe_segment_pad_offsets, kcap >= pad[G] from moe_padded_rows_cap); rows past a
+ * segment's end hold code 0.  Scales are [kcap/128][C], one per (row block, column). */
+
+/* The gate/up GEMM of a training forward: moe_gate_up_fp8, and also the SwiGLU inputs
+ * g, u cached in E4M3 with 1x128 scales (the fp8_quant_1x128 rule):
+ *   guq: uint8 [rows][2f], columns [0, f) = g, [f, 2f) = u;  sgu: FP32 [2f/128][rows]. */
+int moe_gate_up_fp8_train(const uint8_t* xq_rows, const float* sx_rows, const int32_t* offsets,
+                          int rows, const uint8_t* w13, const float* s13, int n_segments, int d,
+                          int f, uint8_t* hq, float* sh, uint8_t* guq, float* sgu,
+                          int32_t* dev_status, void* stream);
+
+/* Setup helper: the transposed FP8 weights of the Dgrad GEMMs.  wT[g][c][r] = w[g][r][c]
+ * and sT[g][cb][rb] = s[g][rb][cb]: a 128x128 block keeps its scale under transposition,
+ * so no requantisation is needed.  With gate_up_interleaved, w is moe_swiglu_fp8_fwd's
+ * w13 (gate and up rows alternating in 64-row blocks) and the output columns come out
+ * gate first: wT = [W1; W3]^T [G][d][2f].  w: uint8 [G][rows][cols]; s: FP32
+ * [G][rows/128][cols/128]; rows, cols % 128 == 0 (rows % 256 when interleaved). */
+int fp8_transpose_128x128(const uint8_t* w, const float* s, int G, int rows, int cols,
+                          int gate_up_interleaved, uint8_t* wT, float* sT, void* stream);
+
+/* Host helper: a bound of the padded row count, ceil((rows + 127 G) / 128) * 128 (-1 on
+ * a bad argument). */
+int moe_padded_rows_cap(int rows, int G);
+
+/* pad[0] = 0, pad[e+1] = pad[e] + ceil(count_e / 128) * 128 with count_e =
+ * offsets[e+1] - offsets[e] (device int32 [G+1] -> [G+1]).  A negative count sets
+ * MOE_ERR_DEVICE_DATA.  G <= 1024. */
+int moe_segment_pad_offsets(const int32_t* offsets, int G, int32_t* pad, int32_t* dev_status,
+                            void* stream);
+
+/* Gradient of moe_combine w.r.t. the expert output rows: dy_rows[row_of[t][k]] =
+ * bf16(fl32(topk_gate[t][k] * dy[t])) and, when shared_row_base >= 0, dy_rows[shared_row_base
+ * + t] = dy[t].  dy: BF16 [T][d]; dy_rows: BF16 [n_rows][d].  A row outside [0, n_rows) sets
+ * MOE_ERR_DEVICE_DATA and is skipped.  d % 8 == 0, K <= 32, 16-byte aligned. */
+int moe_combine_bwd_rows(const uint16_t* dy, const float* topk_gate, const int32_t* row_of,
+                         int T, int K, int d, int shared_row_base, int n_rows, uint16_t* dy_rows,
+                         int32_t* dev_status, void* stream);
+
+/* 128x1 regrouping: the rows of segment order (row r is src[rows[r]], or src[r] when rows
+ * is NULL) quantised in 128x1 tiles with power-of-two scales (the smallest 2^k >= 2^-126
+ * with 448 * 2^k >= the column's max |x| over the block; 1 for an all-zero column), stored
+ * transposed: qT uint8 [cols][kcap], sT FP32 [kcap/128][cols], padded layout as above.
+ * src: BF16 [src_rows][cols]; offsets [G+1] and pad [G+1] on the device.  A gathered row
+ * outside [0, src_rows) sets MOE_ERR_DEVICE_DATA.  cols % 128 == 0, kcap % 128 == 0,
+ * G <= 1024, src and qT 16-byte aligned. */
+int fp8_quant_128x1_pow2(const uint16_t* src, int src_rows, const int32_t* rows, int cols,
+                         const int32_t* offsets, const int32_t* pad, int G, int kcap,
+                         uint8_t* qT, float* sT, int32_t* dev_status, void* stream);
+
+/* SwiGLU backward with recomputation, per row r of segment order:
+ *   g = fl32(dec(guq[r][c]) * s), u likewise (the cache of moe_gate_up_fp8_train);
+ *   sig = 1 / (1 + expf(-g));  h = g sig u;  dU = dh g sig;  dG = dh u sig (1 + g (1 - sig))
+ * (FP32), written as
+ *   dguq uint8 [rows][2f] (dG columns first) with 1x128 scales sdgu [2f/128][rows] (the
+ *        fp8_quant_1x128 rule) -- the gate/up Dgrad operand;
+ *   hT uint8 [f][kcap], shT [kcap/128][f] and dguT uint8 [2f][kcap], sdguT [kcap/128][2f]
+ *        in 128x1 power-of-two tiles, padded layout as above -- the Wgrad operands.
+ * dh: BF16 [rows][f].  f % 128 == 0, kcap % 128 == 0, G <= 1024. */
+int moe_swiglu_bwd_fp8(const uint8_t* guq, const float* sgu, const uint16_t* dh, int rows, int f,
+                       const int32_t* offsets, const int32_t* pad, int G, int kcap,
+                       uint8_t* dguq, float* sdgu, uint8_t* hT, float* shT, uint8_t* dguT,
+                       float* sdguT, void* stream);
+
+/* Wgrad: for every expert e, dW[e][i][j] = sum over e's row blocks rb of saT[rb][i] *
+ * sbT[rb][j] * sum_{p in rb} dec(aT[i][p]) * dec(bT[j][p]), FP32, on tcgen05 tensor cores
+ * with the power-of-two block scales applied by the hardware (kind::mxf8f6f4): one scale
+ * per (row block, output row) and per (row block, output column), each row block's
+ * product promoted with its own scales.  An expert without rows gets zeros.
+ * aT uint8 [I][kcap], saT FP32 [kcap/128][I]; bT uint8 [J][kcap], sbT FP32 [kcap/128][J];
+ * pad [G+1] (device); dW FP32 [G][I][J].  Scales must be positive normal powers of two
+ * (else MOE_ERR_DEVICE_DATA); pad must start at 0, rise in whole 128-row blocks and stay
+ * within kcap (else MOE_ERR_DEVICE_DATA).  I, J, kcap % 128 == 0; G <= 1024. */
+int fp8_wgrad_grouped_gemm(const uint8_t* aT, const float* saT, const uint8_t* bT,
+                           const float* sbT, const int32_t* pad, int G, int I, int J, int kcap,
+                           float* dW, int32_t* dev_status, void* stream);
+
 /* ---- combine and bias update ------------------------------------------------------- */
 
 /* y[t] = bf16( y_rows[shared_row_base + t] + sum_{k=0..K-1} gate[t][k] * y_rows[row_of[t][k]] )

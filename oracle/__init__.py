@@ -47,7 +47,7 @@ from .permute import permute
 from .gemm import blockscaled_gemm, swiglu_expert, combine
 from .layer import moe_layer, moe_layer_tokens
 from .balance import plain_topk, seq_balance_stats
-from .backward import (padded_offsets, quant_128x1_pow2_segments, wgrad, swiglu_backward,
+from .backward import (combine_backward_rows, padded_offsets, quant_128x1_pow2_segments, wgrad, swiglu_backward,
                        dequant_rows_1x128_f32, swiglu_cache, expert_backward)
 
 __all__ = [
@@ -56,6 +56,6 @@ __all__ = [
     "dequant_128x128", "quant_1x128_pow2", "quant_128x128_pow2", "router_logits", "sigmoid_f32", "route", "route_token",
     "bias_update", "permute", "blockscaled_gemm", "swiglu_expert", "combine",
     "moe_layer", "moe_layer_tokens", "plain_topk", "seq_balance_stats",
-    "padded_offsets", "quant_128x1_pow2_segments", "wgrad", "swiglu_backward",
+    "combine_backward_rows", "padded_offsets", "quant_128x1_pow2_segments", "wgrad", "swiglu_backward",
     "dequant_rows_1x128_f32", "swiglu_cache", "expert_backward",
 ]

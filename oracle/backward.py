@@ -58,6 +58,22 @@ from .quant import quant_1x128, _pow2_scale_from_amax
 from .gemm import blockscaled_gemm
 
 
+def combine_backward_rows(dy, gate, row_of, shared_row_base, n_rows):
+    """Gradient of the combine y_t = Y[shared_row_base + t] + sum_k g_tk * Y[row_of[t, k]]
+    with respect to the expert output rows, as the expert backward's BF16 input:
+    dY[row_of[t, k]] = bf16(fl32(g_tk * dy_t)), dY[shared_row_base + t] = dy_t (float32
+    array of BF16 values; rows nobody uses stay 0)."""
+    dy = np.asarray(dy, np.float32)
+    T, d = dy.shape
+    out = np.zeros((n_rows, d), np.float32)
+    for t in range(T):
+        if shared_row_base >= 0:
+            out[shared_row_base + t] = dy[t]
+        for k in range(row_of.shape[1]):
+            out[row_of[t, k]] = bf16_round((np.float32(gate[t, k]) * dy[t]).astype(np.float32))
+    return out
+
+
 def padded_offsets(seg):
     """Start of every expert's 128-row-aligned block range: pad[e] = sum over e' < e of
     ceil(count_e' / 128) * 128; pad[G] = R_pad."""

@@ -201,6 +201,29 @@ def _sampled_outputs(cfg, layer, x, bias, tokens, i_ref, pow2=False):
                                    pow2=pow2)
 
 
+def _steered_tokens(cfg, layer, same, rng, n):
+    """n tokens (routed identically on both sides) chosen where a GEMM tile edge can break:
+    the last row of segments whose length is off the 128-row grid, the first and last rows
+    of the busiest expert, the last token (the shared segment's last M tile, partly filled
+    when T % 128 != 0) and tokens on 1-row segments; random tokens fill the rest."""
+    counts = layer.counts.cpu().numpy()
+    offs = layer.offsets.cpu().numpy()
+    row_token = layer.row_token.cpu().numpy()
+    picks = []
+    ragged = [e for e in range(cfg.E) if counts[e] % 128 != 0]
+    for e in rng.permutation(ragged)[:4]:
+        picks.append(int(row_token[offs[e + 1] - 1]))
+    hot = int(np.argmax(counts))
+    picks += [int(row_token[offs[hot]]), int(row_token[offs[hot + 1] - 1])]
+    picks.append(cfg.T - 1)
+    for e in [e for e in range(cfg.E) if counts[e] == 1][:2]:
+        picks.append(int(row_token[offs[e]]))
+    picks = [t for t in dict.fromkeys(picks) if same[t]]
+    rest = np.setdiff1d(np.nonzero(same)[0], picks)
+    picks += rng.choice(rest, max(0, n - len(picks)), replace=False).tolist()
+    return sorted(picks[:max(n, len(picks))])
+
+
 def _check_config(cfg, w, n_sample, mx=False):
     x = workloads.gen_x(cfg)
     layer = MoELayer(cfg, w, mx=mx)
@@ -218,8 +241,7 @@ def _check_config(cfg, w, n_sample, mx=False):
         for got, want in zip((layer.counts, layer.offsets, layer.row_token, layer.row_of), ref):
             assert np.array_equal(got.cpu().numpy(), want)
     rng = np.random.default_rng(cfg.T)
-    cand = np.nonzero(same)[0]
-    tokens = sorted(rng.choice(cand, n_sample, replace=False).tolist())
+    tokens = _steered_tokens(cfg, layer, same, rng, n_sample)
     part = _sampled_outputs(cfg, layer, x, bias, tokens, i_ref, pow2=mx)
     y = bf16_to_f32(layer.y)[tokens]
     assert_close(y, part["y"], what=f"{cfg.name} sampled tokens" + (" (MX)" if mx else ""))
@@ -227,11 +249,11 @@ def _check_config(cfg, w, n_sample, mx=False):
 
 
 def test_v3_layer(v3_weights):
-    _check_config(workloads.V3, v3_weights, n_sample=4)
+    _check_config(workloads.V3, v3_weights, n_sample=16)
 
 
 def test_decode_layer(v3_weights):
-    _check_config(workloads.DECODE, v3_weights, n_sample=4)
+    _check_config(workloads.DECODE, v3_weights, n_sample=16)
 
 
 def test_skewed_layer_and_bias_update(v3_weights):
@@ -240,9 +262,11 @@ def test_skewed_layer_and_bias_update(v3_weights):
     saved = w.bias.clone()
     try:
         w.bias.copy_(workloads.gen_bias(cfg).to(DEV))
-        layer = _check_config(cfg, w, n_sample=3)
+        layer = _check_config(cfg, w, n_sample=16)
         counts = layer.counts.cpu().numpy()
-        assert counts.max() / counts.mean() > 4          # Zipf-shaped popularity
+        # the workload's calibrated skew (10x on the oracle's routing; near-ties may move
+        # a few pairs on the GPU's own logits)
+        assert 9.0 <= counts.max() / counts.mean() <= 11.0
         before = w.bias.cpu().numpy().copy()
         layer.bias_update(0.001)
         assert np.array_equal(w.bias.cpu().numpy(),
@@ -291,7 +315,7 @@ def test_tiny_mx_layer_from_identical_logits():
 def test_v3_mx_layer_sampled_tokens():
     w = make_weights(workloads.V3, DEV, pow2=True)
     try:
-        _check_config(workloads.V3, w, n_sample=3, mx=True)
+        _check_config(workloads.V3, w, n_sample=16, mx=True)
     finally:
         del w
         torch.cuda.empty_cache()

@@ -169,3 +169,23 @@ def test_expert_backward_zero_gradient_is_zero():
     out = oracle.expert_backward(seg, x, np.zeros_like(dy), guq, sgu, experts)
     for k in ("dh", "dg", "du", "dx", "dw1", "dw3", "dw2"):
         assert (out[k] == 0).all(), k
+
+
+def test_combine_backward_rows_matches_autograd():
+    """The rows' gradient of the combine, from torch autograd of the combine itself (float64),
+    rounded to BF16 the way the expert backward takes it."""
+    rng = _rng(6)
+    T, K, d = 7, 3, 16
+    row_of = rng.permutation(T * K).reshape(T, K).astype(np.int32)
+    gate = rng.uniform(0.05, 1.0, (T, K)).astype(np.float32)
+    dy = torch.tensor(rng.standard_normal((T, d)), dtype=torch.float32).to(torch.bfloat16)
+    Y = torch.zeros(T * K + T, d, dtype=torch.float64, requires_grad=True)
+    y = Y[T * K:T * K + T] + sum(torch.tensor(gate[:, k], dtype=torch.float64)[:, None] *
+                                 Y[torch.tensor(row_of[:, k], dtype=torch.long)] for k in range(K))
+    y.backward(dy.double())
+    got = oracle.combine_backward_rows(dy.float().numpy(), gate, row_of, T * K, T * K + T)
+    ref = Y.grad.numpy()
+    assert np.array_equal(got[T * K:], dy.float().numpy())        # the shared rows: dy itself
+    # the routed rows: the exact product rounded once to BF16 (at most half a BF16 ulp)
+    assert (np.abs(got - ref) <= np.abs(ref) * 2.0 ** -8 + 1e-30).all()
+    assert np.array_equal(got, oracle.bf16_round(got))

@@ -53,3 +53,22 @@ def routing_margin(c_row, idx_row, n_groups, topk_groups, group_topn):
     rest = np.setdiff1d(allowed, idx_row)
     gap_e = float(c_row[idx_row].min()) - float(c_row[rest].max()) if rest.size else np.inf
     return min(gap_g, gap_e)
+
+
+def assert_fp8_decoded_close(got, ref, scale, what="", max_diff_frac=0.01, mae=MAE_REL):
+    """Decoded FP8 tensors from two computations whose inputs differ in their last FP32
+    bits: a value may land on the other side of an E4M3 rounding boundary, so each element
+    may differ by one E4M3 step (1/8 of the value for normal codes, scale * 2^-9 in the
+    subnormal range); few codes differ (beyond group scales an FP32 ulp apart), and the
+    mean error stays within `mae` of the RMS.  `scale`: each element's group scale (broadcastable)."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    scale = np.broadcast_to(np.asarray(scale, np.float64), ref.shape)
+    err = np.abs(got - ref)
+    bound = 0.125 * np.abs(ref) + scale * 2.0 ** -9
+    assert (err <= bound * (1 + 1e-6)).all(), f"{what}: an element moved by more than one E4M3 step"
+    # a code change moves a value by >= 1/16 of it; a scale an FP32 ulp apart by ~1e-7
+    moved = (err > 1e-4 * np.abs(ref) + scale * 2.0 ** -12).mean()
+    assert moved <= max_diff_frac, f"{what}: {moved:.3%} of the codes differ"
+    rms = np.sqrt(np.mean(ref ** 2)) or 1.0
+    assert err.mean() / rms <= mae, f"{what}: mae/rms={err.mean() / rms:.3e}"

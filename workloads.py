@@ -59,7 +59,10 @@ TINY = MoEConfig("tiny", T=256, d=512, E=16, n_groups=4, topk_groups=2, K=4, f=2
                  n_outlier=4, outlier_scale=20.0, w_std=0.02)
 V3 = MoEConfig("v3", T=4096, d=7168, E=256, n_groups=8, topk_groups=4, K=8, f=2048,
                n_outlier=72, outlier_scale=30.0, w_std=0.006)
-SKEWED = replace(V3, name="skewed", T=16384, zipf_s=1.1, zipf_beta=0.35)
+# beta: bisected on the oracle router over this workload's own x, centroids and bias so
+# that the busiest expert takes 10x the mean load (the workload's "up to ~10x mean load on
+# hot experts"); tests/test_workloads.py checks the ratio
+SKEWED = replace(V3, name="skewed", T=16384, zipf_s=1.1, zipf_beta=0.0176)
 DECODE = replace(V3, name="decode", T=128)
 # V3 shapes with 32 experts and 512 tokens (about 128 rows per expert, like V3): a small
 # case for profiler captures (1.4 GB of expert weights).
