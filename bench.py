@@ -1,7 +1,8 @@
 """Benchmark of the MoE FFN layer forward (DeepSeek-V3 shape) on B300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--config v3|decode|skewed|tiny|sweep|sweep_mx]
+                    [--config v3|decode|skewed|tiny|v3_e32|sweep|sweep_mx] [--mx]
+                    [--backward] [--tiling auto|single|pair]
 
 One step is one pass of the whole hot path over one batch: router logits, routing,
 permutation, 1x128 quantisation, row gather, gate/up grouped GEMM with fused SwiGLU and
@@ -51,13 +52,15 @@ def parse():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", choices=["v3", "decode", "skewed", "tiny", "v3_e32", "sweep",
-                                         "sweep_mx"],
+    ap.add_argument("--config", choices=["v3", "decode", "skewed", "tiny", "v3_e32", "decode_e32",
+                                         "sweep", "sweep_mx"],
                     default="v3")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--mx", action="store_true",
                     help="layer configs: the MX-native variant (power-of-two scales applied by "
                          "the tensor core) instead of FP32 scales with software promotion")
+    ap.add_argument("--backward", action="store_true",
+                    help="layer configs: time a training step (forward + expert backward)")
     ap.add_argument("--tiling", choices=["auto", "single", "pair"], default="auto",
                     help="CTA tiling of the FP32-scale grouped GEMM (moe_set_gemm_tiling)")
     ap.add_argument("--shape", default=None,
@@ -313,28 +316,65 @@ def run_layer(args, cfg, rank, world, dev):
             stage_ms[n1] += e0.elapsed_time(e1)
     stage_ms = {k: v / args.steps for k, v in stage_ms.items()}
 
-    # end to end through the public API: pinned host x in, pinned host y out, every step
-    y_host = torch.empty(T, cfg.d, dtype=torch.bfloat16).pin_memory()
-    barrier(world)
+    # End to end through the public API: every step copies its input x from pinned host
+    # memory and reads its output y back to pinned host memory.  x and y are double
+    # buffered so that step i+1's input copy and step i-1's output copy run on their own
+    # streams while step i computes; events order each copy against the compute that
+    # uses or overwrites its buffer.
+    y_host = [torch.empty(T, cfg.d, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    xb = [torch.empty_like(x) for _ in range(2)]
+    yb = [torch.empty(T, cfg.d, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    comp = torch.cuda.current_stream()
+    h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()
+    x_ready, x_free = [ev(), ev()], [ev(), ev()]
+    y_ready, y_free = [ev(), ev()], [ev(), ev()]
+
+    def e2e_step(i):
+        j = i % 2
+        with torch.cuda.stream(h2d):
+            if i >= 2:
+                h2d.wait_event(x_free[j])              # step i-2 has read this buffer
+            xb[j].copy_(x_host, non_blocking=True)
+            x_ready[j].record(h2d)
+        comp.wait_event(x_ready[j])
+        if i >= 2:
+            comp.wait_event(y_free[j])                 # step i-2's output has left
+        if skewed:
+            w.bias.copy_(bias0)
+            layer.forward(xb[j])
+            layer.bias_update(GAMMA)
+        layer.forward(xb[j], out=yb[j])
+        x_free[j].record(comp)
+        y_ready[j].record(comp)
+        with torch.cuda.stream(d2h):
+            d2h.wait_event(y_ready[j])
+            y_host[j].copy_(yb[j], non_blocking=True)
+            y_free[j].record(d2h)
+
+    for i in range(2):                                 # warm the streams and events
+        e2e_step(i)
     torch.cuda.synchronize()
+    barrier(world)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(args.steps):
-        x.copy_(x_host, non_blocking=True)
-        procedure()
-        y_host.copy_(layer.y, non_blocking=True)
-    e1.record()
+    e0.record(h2d)
+    for i in range(args.steps):
+        e2e_step(i)
+    comp.wait_stream(d2h)
+    e1.record(comp)
     torch.cuda.synchronize()
     barrier(world)
     ms_e2e = max_over_ranks(e0.elapsed_time(e1), world)
     layer.check_status()
+    assert torch.equal(y_host[(args.steps - 1) % 2], yb[(args.steps - 1) % 2].cpu())
 
     counts = layer.counts.cpu().numpy()
     return dict(ms_total=ms_total, stage_ms=stage_ms, ms_e2e=ms_e2e, clocks=clocks.summary(),
                 counts=counts, launches=launches_per_step * args.steps,
                 forwards_per_step=2 if skewed else 1,
-                h2d=x_host.numel() * 2, d2h=y_host.numel() * 2, layer=layer, weights=w, x=x_host)
+                h2d=x_host.numel() * 2, d2h=y_host[0].numel() * 2, layer=layer, weights=w,
+                x=x_host)
 
 
 def _oracle_token_times(payload):
@@ -519,6 +559,92 @@ def main_ours(args, cfg, rank, world, dev):
         print(json.dumps(out), flush=True)
 
 
+def main_backward(args, cfg, rank, world, dev):
+    """A training step of the layer's experts: the training forward (SwiGLU inputs cached
+    in FP8) and the expert backward (Dgrad and Wgrad of all three matrices, 128x1
+    regrouping, SwiGLU recompute) from a seeded dy.  One JSON line; stage times from CUDA
+    events; the roofline is the gate/up Wgrad's."""
+    from fp8_block_scaled_bias_b300 import MoELayer, make_weights
+    pk = peaks()
+    T = cfg.T
+    w = make_weights(cfg, dev)
+    x = workloads.gen_x(cfg, base_seed=rank).to(dev)
+    g = torch.Generator().manual_seed(1000 + rank)
+    dy = (torch.randn(T, cfg.d, generator=g) * 0.1).to(torch.bfloat16).to(dev)
+    layer = MoELayer(cfg, w, train=True)
+    layer.transposed_weights()                              # setup, not timed
+
+    def step(marks=None):
+        mk = None
+        if marks is not None:
+            def mk(name):
+                e = torch.cuda.Event(enable_timing=True)
+                e.record()
+                marks.append((name, e))
+        layer.forward(x, mark=mk)
+        return layer.backward(dy, mark=mk)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    layer.check_status()
+    all_marks = []
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clocks:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(args.steps):
+            e = torch.cuda.Event(enable_timing=True)
+            e.record()
+            marks = [("start", e)]
+            out = step(marks)
+            all_marks.append(marks)
+        t1.record()
+        torch.cuda.synchronize()
+    barrier(world)
+    ms_total = max_over_ranks(t0.elapsed_time(t1), world)
+    layer.check_status()
+    stage_ms = {}
+    for marks in all_marks:
+        for (n0, e0), (n1, e1) in zip(marks[:-1], marks[1:]):
+            stage_ms[n1] = stage_ms.get(n1, 0.0) + e0.elapsed_time(e1) / args.steps
+    counts = layer.counts.cpu().numpy()
+    rows, kpad = layer.rows, int(out["pad"][-1].item())
+    d, f, G = cfg.d, cfg.f, cfg.E + 1
+    cl = clocks.summary()
+    fp8_peak, peak_note = fp8_peak_for(pk, cl)
+    wg_flops = 2 * rows * 2 * f * d
+    wg_bytes = 2 * f * kpad + d * kpad + kpad // 128 * (2 * f + d) * 4 + G * 2 * f * d * 4
+    roof = kernel_roofline("fp8_mx_gemm_kernel<F32> (gate/up Wgrad)", wg_bytes, wg_flops,
+                           stage_ms["gate_up_wgrad"], pk, fp8_peak)
+    roof["traffic"] = None
+    train_flops = 3 * cfg.flops()               # forward + Dgrad + Wgrad of each matrix
+    ms_step = ms_total / args.steps
+    out_line = {
+        "metric": "MoE-layer training step (forward + expert backward) tokens/s",
+        "value": round(T * world * args.steps / (ms_total / 1e3), 1), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp8_e4m3", "data": "synthetic",
+        "config": {"workload": f"DeepSeek-V3-shape MoE layer ({cfg.name}): T={T}, d_model={d}, "
+                               f"{cfg.E} routed experts, top-{cfg.K}, d_ffn={f}, 1 shared "
+                               f"expert; training forward + expert backward (router and gate "
+                               f"gradients not computed); dy ~ N(0, 0.1) BF16",
+                   "tokens_per_gpu": T, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2"},
+        "fp8_tflops": round(train_flops * world * args.steps / (ms_total / 1e3) / 1e12, 1),
+        "roofline": roof,
+        "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
+        "active_experts": int((counts > 0).sum()),
+        "gpu_launches": (sum(layer.STAGE_LAUNCHES.values()) + layer.BACKWARD_LAUNCHES) * args.steps,
+        "clocks": cl,
+    }
+    if rank == 0:
+        print(json.dumps(out_line), flush=True)
+
+
 def main_reference(args, cfg, rank, world, dev):
     if rank != 0:
         return
@@ -636,6 +762,8 @@ def main():
     lib.moe_set_gemm_tiling({"auto": 0, "single": 1, "pair": 2}[args.tiling])
     if args.config in ("sweep", "sweep_mx"):
         main_sweep(args, rank, dev, mx=args.config == "sweep_mx")
+    elif args.backward:
+        main_backward(args, workloads.CONFIGS[args.config], rank, world, dev)
     else:
         main_ours(args, workloads.CONFIGS[args.config], rank, world, dev)
     if world > 1:

@@ -128,8 +128,8 @@ class MoELayer:
     STAGE_LAUNCHES = {"router_logits": 1, "route": 1, "permute": 3, "quant_dispatch": 1,
                       "gate_up": 1, "down": 1, "combine": 1}
 
-    def forward(self, x, logits=None, residual=False, mark=None):
-        """x BF16 [T, d] on the device -> y BF16 [T, d] (the layer's own buffer).
+    def forward(self, x, logits=None, residual=False, mark=None, out=None):
+        """x BF16 [T, d] on the device -> y BF16 [T, d] (the layer's own buffer, or ``out``).
 
         ``mark(name)``, if given, is called after each stage's launches (the bench records
         a CUDA event there)."""
@@ -162,11 +162,12 @@ class MoELayer:
         down(self.hq, self.sh, w.w2, w.s2, self.offsets, self.rows, status=self.status,
              out=self.y_rows)
         mark("down")
-        ops.combine(self.y_rows, self.row_of, self.gate, self.T * cfg.K, self.status, out=self.y)
+        y = self.y if out is None else out
+        ops.combine(self.y_rows, self.row_of, self.gate, self.T * cfg.K, self.status, out=y)
         mark("combine")
         if residual:
-            return self.y + x
-        return self.y
+            return y + x
+        return y
 
     # kernel launches of one backward
     BACKWARD_LAUNCHES = 11
@@ -184,8 +185,8 @@ class MoELayer:
     def backward(self, dy, mark=None):
         """dy BF16 [T, d] (gradient of the layer output) -> dict of dx BF16 [T, d] (through
         the experts, not the router), dw13 FP32 [E+1, 2f, d] ([dW1; dW3], gate rows first)
-        and dw2 FP32 [E+1, d, f], plus the intermediate tensors.  Needs a forward with
-        train=True on the same layer first."""
+        and dw2 FP32 [E+1, d, f], plus the intermediate tensors (the layer's own buffers,
+        overwritten by the next backward).  Needs a forward with train=True first."""
         if not self.train or self.x is None:
             raise RuntimeError("backward needs a forward of a layer built with train=True")
         cfg, T, K, E = self.cfg, self.T, self.cfg.K, self.cfg.E
@@ -193,28 +194,49 @@ class MoELayer:
         mark = mark or (lambda name: None)
         w2T, s2T, w13T, s13T = self.transposed_weights()
         st = self.status
-        dy_rows = ops.combine_bwd_rows(dy, self.gate, self.row_of, T * K, rows, status=st)
-        dyq, sdy = ops.quant_1x128(dy_rows)
-        dh = ops.grouped_gemm(dyq, sdy, w2T, s2T, self.offsets, rows, status=st)
+        b = self._backward_buffers(dy.device)
+        kcap = b["kcap"]
+        ops.combine_bwd_rows(dy, self.gate, self.row_of, T * K, rows, status=st, out=b["dy_rows"])
+        ops.quant_1x128(b["dy_rows"], out=(b["dyq"], b["sdy"]))
+        ops.grouped_gemm(b["dyq"], b["sdy"], w2T, s2T, self.offsets, rows, status=st, out=b["dh"])
         mark("down_dgrad")
-        kcap = ops.padded_rows_cap(rows, G)
-        pad = ops.segment_pad_offsets(self.offsets, G, status=st)
-        dguq, sdgu, hT, shT, dguT, sdguT = ops.swiglu_bwd(self.guq, self.sgu, dh, self.offsets,
-                                                          pad, kcap)
+        ops.segment_pad_offsets(self.offsets, G, status=st, out=b["pad"])
+        ops.swiglu_bwd(self.guq, self.sgu, b["dh"], self.offsets, b["pad"], kcap,
+                       out=(b["dguq"], b["sdgu"], b["hT"], b["shT"], b["dguT"], b["sdguT"]))
         mark("swiglu_bwd")
-        dx_rows = ops.grouped_gemm(dguq, sdgu, w13T, s13T, self.offsets, rows, status=st)
-        dx = ops.combine(dx_rows, self.row_of, self._ones, T * K, st)   # gates of 1
+        ops.grouped_gemm(b["dguq"], b["sdgu"], w13T, s13T, self.offsets, rows, status=st,
+                         out=b["dx_rows"])
+        ops.combine(b["dx_rows"], self.row_of, self._ones, T * K, st, out=b["dx"])  # gates 1
         mark("gate_up_dgrad")
-        dyT, sdyT = ops.quant_128x1_pow2(dy_rows, self.offsets, pad, kcap, status=st)
-        dw2 = ops.wgrad(dyT, sdyT, hT, shT, pad, status=st)
+        ops.quant_128x1_pow2(b["dy_rows"], self.offsets, b["pad"], kcap, status=st,
+                             out=(b["dyT"], b["sdyT"]))
+        ops.wgrad(b["dyT"], b["sdyT"], b["hT"], b["shT"], b["pad"], status=st, out=b["dw2"])
         mark("down_wgrad")
-        xT, sxT = ops.quant_128x1_pow2(self.x, self.offsets, pad, kcap, rows=self.row_token,
-                                       status=st)
-        dw13 = ops.wgrad(dguT, sdguT, xT, sxT, pad, status=st)
+        ops.quant_128x1_pow2(self.x, self.offsets, b["pad"], kcap, rows=self.row_token,
+                             status=st, out=(b["xT"], b["sxT"]))
+        ops.wgrad(b["dguT"], b["sdguT"], b["xT"], b["sxT"], b["pad"], status=st, out=b["dw13"])
         mark("gate_up_wgrad")
-        return dict(dx=dx, dw13=dw13, dw2=dw2, dy_rows=dy_rows, dh=dh, dx_rows=dx_rows,
-                    pad=pad, kcap=kcap, dguq=dguq, sdgu=sdgu, hT=hT, shT=shT, dguT=dguT,
-                    sdguT=sdguT, dyT=dyT, sdyT=sdyT, xT=xT, sxT=sxT)
+        return b
+
+    def _backward_buffers(self, dev):
+        """The backward's outputs and intermediates, allocated on the first backward."""
+        if getattr(self, "_bwd", None) is None:
+            cfg, T, E, d, f = self.cfg, self.T, self.cfg.E, self.cfg.d, self.cfg.f
+            rows, G = self.rows, E + 1
+            kcap = ops.padded_rows_cap(rows, G)
+            emp = lambda *sh, dt=torch.float32: torch.empty(*sh, dtype=dt, device=dev)
+            u8, bf, i32 = torch.uint8, torch.bfloat16, torch.int32
+            self._bwd = dict(
+                kcap=kcap, dy_rows=emp(rows, d, dt=bf), dyq=emp(rows, d, dt=u8),
+                sdy=emp(d // 128, rows), dh=emp(rows, f, dt=bf), pad=emp(G + 1, dt=i32),
+                dguq=emp(rows, 2 * f, dt=u8), sdgu=emp(2 * f // 128, rows),
+                hT=emp(f, kcap, dt=u8), shT=emp(kcap // 128, f),
+                dguT=emp(2 * f, kcap, dt=u8), sdguT=emp(kcap // 128, 2 * f),
+                dx_rows=emp(rows, d, dt=bf), dx=emp(T, d, dt=bf),
+                dyT=emp(d, kcap, dt=u8), sdyT=emp(kcap // 128, d),
+                xT=emp(d, kcap, dt=u8), sxT=emp(kcap // 128, d),
+                dw2=emp(G, d, f), dw13=emp(G, 2 * f, d))
+        return self._bwd
 
     def bias_update(self, gamma):
         """Aux-loss-free bias step from this forward's expert loads (in place)."""

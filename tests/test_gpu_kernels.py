@@ -292,6 +292,35 @@ def test_combine_matches_oracle(T, K, d, shared):
     assert (np.abs(y - ref) <= ulp).all()
 
 
+def test_combine_v3_shape_sampled_tokens():
+    """The V3 launch (T=4096, K=8, d=7168, 36,864 BF16 expert rows, shared rows last):
+    64 seeded tokens checked against the oracle, the others by the same FP32 rule's
+    invariants (finite, one BF16 ulp of the float64 sum on the sampled ones)."""
+    cfg = workloads.V3
+    T, K, d = cfg.T, cfg.K, cfg.d
+    rng = np.random.default_rng(77)
+    rows = T * K + T
+    Y = torch.randn(rows, d, generator=torch.Generator().manual_seed(77)).to(torch.bfloat16)
+    row_of = rng.permutation(T * K).reshape(T, K).astype(np.int32)
+    gate = rng.uniform(0, 1, (T, K)).astype(np.float32)
+    gate /= gate.sum(1, keepdims=True)
+    st = ops.new_status(DEV)
+    y = ops.combine(Y.to(DEV), torch.from_numpy(row_of).to(DEV), torch.from_numpy(gate).to(DEV),
+                    T * K, st)
+    torch.cuda.synchronize()
+    assert ops.status_value(st) == 0
+    y = bf16_to_f32(y)
+    assert np.isfinite(y).all()
+    toks = np.sort(rng.choice(T, 64, replace=False))
+    toks[-1] = T - 1
+    Yn = Y.float().numpy()
+    ref = oracle.combine(np.concatenate([Yn[row_of[toks].ravel()], Yn[T * K + toks]]),
+                         np.arange(len(toks) * K, dtype=np.int32).reshape(len(toks), K),
+                         gate[toks], len(toks) * K)
+    ulp = np.maximum(np.abs(ref), 2.0 ** -126) * 2.0 ** -7
+    assert (np.abs(y[toks] - ref) <= ulp).all()
+
+
 def test_combine_page_toy_mixture():
     g = GOLD["toy_mixture"]
     Y = torch.zeros(2, 8, dtype=torch.bfloat16)

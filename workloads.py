@@ -67,7 +67,9 @@ DECODE = replace(V3, name="decode", T=128)
 # V3 shapes with 32 experts and 512 tokens (about 128 rows per expert, like V3): a small
 # case for profiler captures (1.4 GB of expert weights).
 V3_E32 = replace(V3, name="v3_e32", T=512, E=32)
-CONFIGS = {c.name: c for c in (TINY, V3, SKEWED, DECODE, V3_E32)}
+# its decode-shaped counterpart (16 tokens: segments of 0-8 rows) for GEMM captures
+DECODE_E32 = replace(V3, name="decode_e32", T=16, E=32)
+CONFIGS = {c.name: c for c in (TINY, V3, SKEWED, DECODE, V3_E32, DECODE_E32)}
 
 # Standalone FP8 block-scaled GEMM sweep, (M, N, K).
 GEMM_SWEEP = [(4096, 7168, 2048), (4096, 4096, 7168), (8192, 18432, 7168),
