@@ -60,11 +60,12 @@ constexpr uint32_t SF_SLOT_COLS = 16;
 // each B tile (two MMAs per K step, two 128 x 224 accumulators): 60 KB per K block for
 // twice the MMA work of the single tile's 48 KB, so fewer bytes ride the shared-memory
 // ring per multiply-add -- the ring is what bounds these kernels.
-template <bool PAIR>
+template <bool PAIR, bool F32OUT = false>
 struct Tile {
   static constexpr int BM = PAIR ? 256 : 128;       // rows per CTA tile
   static constexpr int BN = PAIR ? 224 : 256;       // columns per accumulator
-  static constexpr int STAGES = PAIR ? 3 : 4;
+  // FP32 output (Wgrad): short K loops, so 3 stages, and room for the store staging
+  static constexpr int STAGES = (PAIR || F32OUT) ? 3 : 4;
   static constexpr int A_BYTES = BM * BK;
   static constexpr int B_BYTES = BN * BK;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -84,7 +85,10 @@ struct Tile {
   static constexpr int OFF_USTART = OFF_SEG + (MAX_G + 1) * 4;
   static constexpr int OFF_WSUM = OFF_USTART + (MAX_G + 1) * 4;
   static constexpr int OFF_AMAX = OFF_WSUM + 32 * 4;         // [2 tiles][2 halves][128 rows]
-  static constexpr int SMEM_USED = OFF_AMAX + 2 * 2 * 128 * 4;
+  // FP32 output: per epilogue warp a [32 rows][36] float staging tile for coalesced stores
+  static constexpr int STG_LD = 36;
+  static constexpr int OFF_STG = OFF_AMAX + 2 * 2 * 128 * 4;
+  static constexpr int SMEM_USED = OFF_STG + (F32OUT ? EPI_WARPS * 32 * STG_LD * 4 : 0);
   static constexpr int SMEM_ALLOC = SMEM_USED + 1024;
   static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 };
@@ -184,7 +188,7 @@ __global__ void __launch_bounds__(mx::THREADS, 1)
     fp8_mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB, const MxParams p) {
   using namespace mx;
-  using TL = Tile<PAIR>;
+  using TL = Tile<PAIR, EPI == kEpiF32>;
   constexpr int BM = TL::BM, BN = TL::BN, STAGES = TL::STAGES;
   constexpr int A_BYTES = TL::A_BYTES, B_BYTES = TL::B_BYTES, STAGE_BYTES = TL::STAGE_BYTES;
   constexpr int OFF_A = TL::OFF_A, OFF_B = TL::OFF_B, OFF_BAR = TL::OFF_BAR;
@@ -474,12 +478,15 @@ __global__ void __launch_bounds__(mx::THREADS, 1)
       int g, m0, rv, nt, kb0, nkb;
       unit_info(unit, g, m0, rv, nt, kb0, nkb);
       if (WG && nkb == 0) {
-        // an expert without rows: its weight gradient is zero (no accumulator use)
+        // an expert without rows: its weight gradient is zero (no accumulator use); each
+        // store instruction writes 512 contiguous bytes of one of the warp's 32 rows
         if (nt * BN + grp * 128 < p.N) {
-          float4* dst = reinterpret_cast<float4*>(
-              p.Cf + (static_cast<long long>(g) * p.M + m0 + row) * p.ldc + nt * BN + grp * 128);
+          float* c0 = p.Cf + (static_cast<long long>(g) * p.M + m0 + q * 32) * p.ldc + nt * BN +
+                      grp * 128 + lane * 4;
 #pragma unroll 8
-          for (int i = 0; i < 32; ++i) dst[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+          for (int r = 0; r < 32; ++r)
+            *reinterpret_cast<float4*>(c0 + static_cast<long long>(r) * p.ldc) =
+                make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         }
         continue;
       }
@@ -489,25 +496,38 @@ __global__ void __launch_bounds__(mx::THREADS, 1)
       tc_fence_after();
       const uint32_t tbase = tmem_base + lane_addr + static_cast<uint32_t>(grp * 128);
       if (WG) {
-        // FP32 weight gradient rows: this thread's row, 128 columns of its half
+        // FP32 weight gradient: the warp's 32 rows x 128 columns of its half, 32 columns at
+        // a time through a shared-memory tile, so each store instruction writes four rows'
+        // 128 contiguous bytes (a row per lane would scatter 16 bytes over 32 rows)
         const bool store = nt * BN + grp * 128 < p.N;
-        float4* dst = reinterpret_cast<float4*>(
-            p.Cf + (static_cast<long long>(g) * p.M + m0 + row) * p.ldc + nt * BN + grp * 128);
+        float* stg = reinterpret_cast<float*>(smem + TL::OFF_STG) +
+                     (warp - EPI_WARP0) * 32 * TL::STG_LD;
+        float* c0 = p.Cf + (static_cast<long long>(g) * p.M + m0 + q * 32) * p.ldc + nt * BN +
+                    grp * 128 + (lane & 7) * 4;
 #pragma unroll
         for (int c = 0; c < 8; c += 2) {
           uint32_t v[2][16];
           tmem_ld_32x32b_x16(tbase + c * 16, v[0]);
           tmem_ld_32x32b_x16(tbase + c * 16 + 16, v[1]);
           tmem_ld_wait();
+          float4* srow = reinterpret_cast<float4*>(stg + lane * TL::STG_LD);
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              srow[h * 4 + i] =
+                  make_float4(__uint_as_float(v[h][4 * i]), __uint_as_float(v[h][4 * i + 1]),
+                              __uint_as_float(v[h][4 * i + 2]), __uint_as_float(v[h][4 * i + 3]));
+          __syncwarp();
           if (store) {
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-              for (int i = 0; i < 4; ++i)
-                dst[(c + h) * 4 + i] =
-                    make_float4(__uint_as_float(v[h][4 * i]), __uint_as_float(v[h][4 * i + 1]),
-                                __uint_as_float(v[h][4 * i + 2]), __uint_as_float(v[h][4 * i + 3]));
+            for (int j = 0; j < 8; ++j) {
+              const int r = 4 * j + (lane >> 3);
+              *reinterpret_cast<float4*>(c0 + static_cast<long long>(r) * p.ldc + c * 16) =
+                  *reinterpret_cast<const float4*>(stg + r * TL::STG_LD + (lane & 7) * 4);
+            }
           }
+          __syncwarp();
         }
       } else if (PAIR) {
         // sub-tile grp (rows 128 grp + row of the block), all BN columns of its accumulator
@@ -633,7 +653,7 @@ bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* ptr
 namespace {
 template <int EPI, bool PAIR>
 int launch_mx_kernel(const uint8_t* A, const uint8_t* B, const MxParams& p, cudaStream_t stream) {
-  using TL = mx::Tile<PAIR>;
+  using TL = mx::Tile<PAIR, EPI == kEpiF32>;
   constexpr bool WG = EPI == kEpiF32;
   CUtensorMap tmA, tmB;
   // Wgrad: A = a^T [M][K] and B = b^T [N][K] shared by every expert; else B is [G][N][K]
