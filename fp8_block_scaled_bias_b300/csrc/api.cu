@@ -247,7 +247,7 @@ int fp8_blockscaled_grouped_gemm(const uint8_t* A, const float* sA, int M_a,
 }
 
 int moe_set_gemm_tiling(int mode) {
-  if (mode < 0 || mode > 2) return MOE_ERR_INVALID_ARG;
+  if (mode < 0 || mode > 3) return MOE_ERR_INVALID_ARG;
   moe::set_gemm_tiling(mode);
   return MOE_OK;
 }

@@ -88,8 +88,12 @@ struct GemmArgs {
   int stall;             // failure-path test: the scheduler waits on a barrier nothing arrives on
 };
 int launch_fp8_gemm(const GemmArgs& a, GemmEpilogue epi, cudaStream_t stream);
+// Grouped GEMM for short segments with the operands swapped (gemm_swap.cu): weight rows on
+// the MMA's M side, 32 tokens on N.  BF16 and SwiGLU epilogues; N % 256 == 0.
+int launch_fp8_gemm_swap(const GemmArgs& a, GemmEpilogue epi, cudaStream_t stream);
 // CTA tiling of the grouped GEMM: 0 automatic, 1 one CTA per 128-row tile, 2 CTA pairs
-// per 256-row tile (tcgen05 cta_group::2).  Process-wide.
+// per 256-row tile (tcgen05 cta_group::2), 3 swapped operands for short segments.
+// Process-wide.
 void set_gemm_tiling(int mode);
 int gemm_tiling();
 

@@ -217,10 +217,16 @@ size_t fp8_grouped_gemm_ws_bytes(int M, int K, int has_a_rows);
 
 /* CTA tiling of fp8_blockscaled_grouped_gemm, moe_gate_up_fp8 and moe_swiglu_fp8_fwd
  * (a performance choice; results are the same bits either way):
- *   0  automatic (the default): tiling 1 (on B300 tiling 2 measured about half as fast);
+ *   0  automatic (the default): tiling 3 when the segments average at most 16 rows
+ *      (M <= 16 * G, decode batches) and N % 256 == 0, else tiling 1 (on B300 tiling 2
+ *      measured about half as fast);
  *   1  one CTA per 128-row x 256-column tile (tcgen05 cta_group::1);
  *   2  two CTAs of a cluster per 256-row x 256-column tile: one tcgen05 cta_group::2
- *      MMA over both CTAs' shared memory, each CTA loading half of the weight tile.
+ *      MMA over both CTAs' shared memory, each CTA loading half of the weight tile;
+ *   3  operands swapped for short segments: 256 weight rows on the MMA's M side times 32
+ *      tokens of a segment on N, so no MMA row is padding; per-expert decode batches are
+ *      small and weight-bound ([sum] core idea 8: transposed GEMM reads).  Needs
+ *      N % 256 == 0; otherwise tiling 1 runs.
  * The setting is process-wide and applies to calls made after it.  Returns
  * MOE_ERR_INVALID_ARG for any other mode. */
 int moe_set_gemm_tiling(int mode);

@@ -1,8 +1,9 @@
 """GPU parity of the tcgen05 block-scaled grouped GEMM (through the C-ABI) against the
 oracle's exact definition: dense and grouped, ragged and empty segments, a half-width
 last N tile, gathered A rows, and the five full-size sweep shapes on sampled rows.  The
-small cases run under both CTA tilings (one CTA per 128-row tile; CTA pairs sharing one
-cta_group::2 MMA per 256-row tile).  The failure path of the bounded waits is exercised
+small cases run under every tiling (one CTA per 128-row tile; CTA pairs sharing one
+cta_group::2 MMA per 256-row tile; swapped operands with weight rows on the MMA's M side,
+which falls back to the first when N % 256 != 0).  The failure path of the bounded waits is exercised
 by a launch whose scheduler waits on a barrier nothing arrives on."""
 
 import numpy as np
@@ -18,7 +19,7 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-@pytest.fixture(params=[1, 2], ids=["single", "pair"])
+@pytest.fixture(params=[1, 2, 3], ids=["single", "pair", "swap"])
 def tiling(request, lib):
     L = lib.load()
     assert L.moe_set_gemm_tiling(request.param) == 0
@@ -192,13 +193,42 @@ def test_grouped_many_ragged_segments_both_tilings_equal(lib):
     L = lib.load()
     outs = []
     try:
-        for mode in (1, 2):
+        for mode in (1, 2, 3):
             L.moe_set_gemm_tiling(mode)
             outs.append(_run(A, sA, B, sB, seg, M))
     finally:
         L.moe_set_gemm_tiling(0)
     assert np.array_equal(outs[0], outs[1])
-    _check(outs[1], _ref(A, sA, B, sB, seg), "40 ragged segments")
+    ref = _ref(A, sA, B, sB, seg)
+    _check(outs[1], ref, "40 ragged segments")
+    # N = 640 is not a multiple of 256: the swapped tiling falls back to the single one
+    assert np.array_equal(outs[2], outs[0])
+
+
+def test_swapped_tiling_short_segments(lib):
+    """Decode-like segments (0 to 40 rows, many of 1-8) on the swapped-operand tiling,
+    N a multiple of 256, against the oracle."""
+    rng = np.random.default_rng(19)
+    counts = rng.integers(0, 9, 60)
+    counts[[2, 7]] = 0
+    counts[[10, 11, 12]] = [1, 32, 40]
+    seg = np.concatenate([[0], np.cumsum(counts)]).tolist()
+    M, N, K, G = seg[-1], 768, 512, len(counts)
+    assert M <= 16 * G                         # the automatic choice picks it too
+    A = _codes(M, K, 51)
+    sA = workloads.gen_scales((K // 128, M), sub_seed=52)
+    B = _codes(G * N, K, 53).view(G, N, K)
+    sB = workloads.gen_scales((G, N // 128, K // 128), sub_seed=54)
+    L = lib.load()
+    try:
+        L.moe_set_gemm_tiling(3)
+        C3 = _run(A, sA, B, sB, seg, M)
+        L.moe_set_gemm_tiling(1)
+        C1 = _run(A, sA, B, sB, seg, M)
+    finally:
+        L.moe_set_gemm_tiling(0)
+    _check(C3, _ref(A, sA, B, sB, seg), "swapped short segments")
+    assert np.abs(C3 - C1).max() <= np.abs(C1).max() * 2.0 ** -7
 
 
 @pytest.mark.parametrize("mode", [1, 2], ids=["single", "pair"])

@@ -117,6 +117,27 @@ def test_tiny_layer_full_path(tiny):
         assert_close(bf16_to_f32(layer.y)[same], ref["y"][same], what="layer output")
 
 
+def test_tiny_layer_on_swapped_tiling(tiny, lib):
+    """The tiny layer with both expert GEMMs on the swapped-operand tiling (weight rows on
+    the MMA's M side, including its SwiGLU epilogue), every intermediate against the
+    oracle from identical logits."""
+    cfg, w, x, ex = tiny
+    g = torch.Generator().manual_seed(5)
+    logits = (torch.randn(cfg.T, cfg.E, generator=g) * 1.5).float()
+    L = lib.load()
+    try:
+        L.moe_set_gemm_tiling(3)
+        layer = MoELayer(cfg, w)
+        layer.forward(x.to(DEV), logits=logits.to(DEV))
+        torch.cuda.synchronize()
+        layer.check_status()
+    finally:
+        L.moe_set_gemm_tiling(0)
+    ref = oracle.moe_layer(x.float().numpy(), w.centroids.cpu().numpy(), w.bias.cpu().numpy(),
+                           ex, cfg.n_groups, cfg.topk_groups, cfg.K, logits=logits.numpy())
+    _compare_tiny(cfg, layer, ref, x)
+
+
 def test_layer_is_deterministic(tiny):
     cfg, w, x, _ = tiny
     layer = MoELayer(cfg, w)
