@@ -238,3 +238,77 @@ def test_tiny_layer_backward_against_oracle(tiny_train):
         assert_close(dw13[e, :f], ref["dw1"][e], what=f"dW1 expert {e}")
         assert_close(dw13[e, f:], ref["dw3"][e], what=f"dW3 expert {e}")
         assert_close(dw2[e], ref["dw2"][e], what=f"dW2 expert {e}")
+
+
+def test_v3_width_backward_sampled(lib):
+    """The backward at V3 width (d=7168, f=2048; 32 experts + the shared one, T=512, top-8):
+    the row gradients bit-exact; the regrouped dY and X of two experts bit-exact; sampled
+    rows of both Dgrads, sampled output rows of both Wgrads (from the GPU's own regrouped
+    operands) and sampled tokens of dx against the oracle."""
+    cfg = workloads.V3_E32
+    T, K, d, f = cfg.T, cfg.K, cfg.d, cfg.f
+    w = make_weights(cfg, DEV)
+    x = workloads.gen_x(cfg)
+    layer = MoELayer(cfg, w, train=True)
+    layer.forward(x.to(DEV))
+    g = torch.Generator().manual_seed(13)
+    dy = (torch.randn(T, d, generator=g) * 0.1).to(torch.bfloat16)
+    out = layer.backward(dy.to(DEV))
+    torch.cuda.synchronize()
+    layer.check_status()
+    seg = layer.offsets.cpu().numpy()
+    row_of, gate = layer.row_of.cpu().numpy(), layer.gate.cpu().numpy()
+    dy_rows = oracle.combine_backward_rows(dy.float().numpy(), gate, row_of, T * K, layer.rows)
+    assert np.array_equal(bf16_to_f32(out["dy_rows"]), dy_rows)
+    pad = oracle.padded_offsets(seg)
+    assert np.array_equal(out["pad"].cpu().numpy(), pad)
+    counts = np.diff(seg)
+    experts = [int(np.argmax(counts[:cfg.E])), cfg.E]        # the busiest and the shared one
+    x_rows = x.float().numpy()[layer.row_token.cpu().numpy()]
+    rng = np.random.default_rng(3)
+    for e in experts:
+        r0, r1, p0, p1 = seg[e], seg[e + 1], pad[e], pad[e + 1]
+        sub = np.array([0, r1 - r0])
+        q_ref, s_ref, _ = oracle.quant_128x1_pow2_segments(dy_rows[r0:r1], sub)
+        assert np.array_equal(out["dyT"].cpu().numpy()[:, p0:p1], q_ref)
+        assert np.array_equal(out["sdyT"].cpu().numpy()[p0 // 128:p1 // 128], s_ref)
+        q_ref, s_ref, _ = oracle.quant_128x1_pow2_segments(x_rows[r0:r1], sub)
+        assert np.array_equal(out["xT"].cpu().numpy()[:, p0:p1], q_ref)
+        assert np.array_equal(out["sxT"].cpu().numpy()[p0 // 128:p1 // 128], s_ref)
+        # Wgrad on sampled output rows, from the GPU's own 128x1 operands
+        wq = [t.cpu().numpy() for t in workloads.gen_expert_f32(cfg, e, device="cuda")]
+        rows_i = np.sort(rng.choice(d, 24, replace=False))
+        ref = oracle.wgrad(out["dyT"].cpu().numpy()[rows_i][:, p0:p1],
+                           out["sdyT"].cpu().numpy()[p0 // 128:p1 // 128][:, rows_i],
+                           out["hT"].cpu().numpy()[:, p0:p1],
+                           out["shT"].cpu().numpy()[p0 // 128:p1 // 128],
+                           np.array([0, p1 - p0]))[0]
+        assert_close(out["dw2"][e].cpu().numpy()[rows_i], ref, what=f"dW2 rows, expert {e}")
+        rows_c = np.sort(rng.choice(2 * f, 24, replace=False))
+        ref = oracle.wgrad(out["dguT"].cpu().numpy()[rows_c][:, p0:p1],
+                           out["sdguT"].cpu().numpy()[p0 // 128:p1 // 128][:, rows_c],
+                           out["xT"].cpu().numpy()[:, p0:p1],
+                           out["sxT"].cpu().numpy()[p0 // 128:p1 // 128],
+                           np.array([0, p1 - p0]))[0]
+        assert_close(out["dw13"][e].cpu().numpy()[rows_c], ref, what=f"dW13 rows, expert {e}")
+        # Dgrads of sampled rows of this expert
+        w1q, s1 = oracle.quant_128x128(wq[0])
+        w3q, s3 = oracle.quant_128x128(wq[1])
+        w2q, s2 = oracle.quant_128x128(wq[2])
+        rr = np.sort(rng.choice(np.arange(r0, r1), min(8, r1 - r0), replace=False))
+        dyq, sdy = oracle.quant_1x128(dy_rows[rr])
+        dh_ref = oracle.bf16_round(oracle.blockscaled_gemm(dyq, sdy, np.ascontiguousarray(w2q.T),
+                                                           np.ascontiguousarray(s2.T)))
+        assert_close(bf16_to_f32(out["dh"])[rr], dh_ref, what=f"dh rows, expert {e}")
+        wcat_t = np.ascontiguousarray(np.concatenate([w1q, w3q], 0).T)
+        scat_t = np.ascontiguousarray(np.concatenate([s1, s3], 0).T)
+        dx_ref = oracle.bf16_round(oracle.blockscaled_gemm(
+            out["dguq"].cpu().numpy()[rr], out["sdgu"].cpu().numpy()[:, rr], wcat_t, scat_t))
+        assert_close(bf16_to_f32(out["dx_rows"])[rr], dx_ref, what=f"dX rows, expert {e}")
+    # dx of sampled tokens: the sum of their rows' dX (unit gates), from the GPU's rows
+    toks = np.sort(rng.choice(T, 16, replace=False))
+    dxr = bf16_to_f32(out["dx_rows"])
+    ref = oracle.combine(np.concatenate([dxr[row_of[toks].ravel()], dxr[T * K + toks]]),
+                         np.arange(16 * K, dtype=np.int32).reshape(16, K),
+                         np.ones((16, K), np.float32), 16 * K)
+    assert_close(bf16_to_f32(out["dx"])[toks], ref, what="dx tokens")
