@@ -17,6 +17,8 @@
 // The 128x1 tiles use power-of-two scales, which the pages give for the regrouped
 // backward tensors; they are quantised from the higher-precision values (BF16 or FP32),
 // one scale per (128-row block, column).  Padded rows of a block hold code 0.
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -46,16 +48,6 @@ MOE_DEV bool block_of(const int32_t* __restrict__ seg, const int32_t* __restrict
 
 // FP32 -> E4M3 byte (round to nearest even, saturating).
 MOE_DEV uint32_t e4m3_byte(float v) { return f32x2_to_e4m3x2(v, 0.0f) & 0xFFu; }
-
-MOE_DEV float e4m3_value(uint32_t code) {
-  // E4M3 fn: bias 7, 3 mantissa bits, subnormals below 2^-6 (codes 0x7F/0xFF are NaN)
-  const uint32_t s = code & 0x80u, e = (code >> 3) & 0xFu, m = code & 7u;
-  float v;
-  if (e == 0) v = static_cast<float>(m) * 0.001953125f;                 // m * 2^-9
-  else v = __uint_as_float(((e + 120u) << 23) | (m << 20));             // 2^(e-7) * 1.m
-  if ((code & 0x7Fu) == 0x7Fu) v = __uint_as_float(0x7FC00000u);
-  return s ? -v : v;
-}
 
 }  // namespace
 
@@ -232,10 +224,23 @@ struct SwigluVals {
   float h, dg, du;
 };
 
-// g, u from their E4M3 codes and 1x128 scales; sigmoid with expf and IEEE division.
-MOE_DEV SwigluVals swiglu_bwd_at(uint32_t qg, uint32_t qu, float sg, float su, float dh) {
-  const float g = __fmul_rn(e4m3_value(qg), sg);
-  const float u = __fmul_rn(e4m3_value(qu), su);
+// Four E4M3 codes (bytes of q, lowest first) -> their exact values (hardware conversion to
+// FP16, which holds every E4M3 value exactly).
+MOE_DEV void e4m3x4_decode(uint32_t q, float (&v)[4]) {
+  uint32_t lo, hi;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(lo) : "h"(static_cast<uint16_t>(q & 0xFFFFu)));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hi) : "h"(static_cast<uint16_t>(q >> 16)));
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&lo));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+  v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+}
+
+// From the decoded g, u codes and their 1x128 scales: g and u (fl32(dec * s)), the sigmoid
+// with expf and IEEE division, h, dG, dU.  (The fast exponential and division move enough
+// dG, dU codes across E4M3 boundaries to cost the gate/up Dgrad its 2e-2 bound.)
+MOE_DEV SwigluVals swiglu_bwd_at(float dg_code, float du_code, float sg, float su, float dh) {
+  const float g = __fmul_rn(dg_code, sg);
+  const float u = __fmul_rn(du_code, su);
   const float sig = __fdiv_rn(1.0f, 1.0f + expf(-g));
   const float silu = g * sig;
   SwigluVals v;
@@ -245,129 +250,133 @@ MOE_DEV SwigluVals swiglu_bwd_at(uint32_t qg, uint32_t qu, float sg, float su, f
   return v;
 }
 
-MOE_DEV void smem_max(float* p, float v) {
-  atomicMax(reinterpret_cast<int*>(p), __float_as_int(v));   // v >= 0: int order = float order
-}
 }  // namespace
 
-// Block (rb, cb): the segment rows of padded block rb, hidden columns [128 cb, 128 cb + 128).
-// Pass 1 finds the row max-abs of dG and dU (their 1x128 groups) and the column max-abs of
-// h, dG and dU (their 128x1 groups); pass 2 recomputes the values and writes the codes.
-__global__ void __launch_bounds__(kBwdThreads) swiglu_bwd_kernel(
+// Block (rb, cb): the segment rows of padded block rb, hidden columns [128 cb, 128 cb + 128),
+// 512 threads.  Warp w owns rows 8 w .. 8 w + 7, lane l columns 4 l .. 4 l + 3, so every
+// value is computed once and kept in registers: the rows' 1x128 max-abs of dG and dU come
+// from a warp reduction per row, the columns' 128x1 max-abs of h, dG and dU from a
+// shared-memory reduction over the 16 warps.  Loads and the row-major stores are
+// coalesced; the transposed codes go out as 8 contiguous bytes per column and thread.
+constexpr int kSwThreads = 512;
+
+__global__ void __launch_bounds__(kSwThreads, 1) swiglu_bwd_kernel(
     const uint8_t* __restrict__ guq, const float* __restrict__ sgu,
     const uint16_t* __restrict__ dh, int R, int f, const int32_t* __restrict__ seg,
     const int32_t* __restrict__ pad, int G, int ldq, uint8_t* __restrict__ dguq,
     float* __restrict__ sdgu, uint8_t* __restrict__ hT, float* __restrict__ shT,
     uint8_t* __restrict__ dguT, float* __restrict__ sdguT) {
-  // dynamic shared memory: the tile's g codes, u codes (rows padded to 144 bytes) and dh
-  // (rows padded to 136 BF16 values), 71,680 bytes
-  extern __shared__ __align__(16) uint8_t bwd_smem[];
-  auto tg = reinterpret_cast<uint8_t(*)[kTile + 16]>(bwd_smem);
-  auto tu = reinterpret_cast<uint8_t(*)[kTile + 16]>(bwd_smem + kTile * (kTile + 16));
-  auto tdh = reinterpret_cast<uint16_t(*)[kTile + 8]>(bwd_smem + 2 * kTile * (kTile + 16));
-  __shared__ float sg_s[kTile], su_s[kTile];
-  __shared__ float rmax_g[kTile], rmax_u[kTile];
-  __shared__ float cpart[3][2][kTile];
+  __shared__ float cpart[16][3][kTile];          // per-warp column max: h, dG, dU
+  __shared__ float cscale[3][kTile];             // the columns' power-of-two scales
   int e, r0, nv;
   if (!block_of(seg, pad, G, blockIdx.x, e, r0, nv)) return;
-  const int cb = blockIdx.y, tid = threadIdx.x;
-  const int NB = f / kTile;                     // 1x128 groups of g (and of u)
-  for (int i = tid; i < kTile * 8; i += kBwdThreads) {   // codes: 8 uint4 per row each
-    const int r = i >> 3, v = i & 7;
-    uint4 a = make_uint4(0, 0, 0, 0), b = a;
-    if (r < nv) {
+  const int cb = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int NB = f / kTile;
+  const int c0 = cb * kTile + 4 * lane;          // this lane's first hidden column
+  float hv[8][4], gv[8][4], uv[8][4];            // h, dG, dU of the warp's 8 rows
+  float cm[3][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  float rs_g[8], rs_u[8];                        // the rows' 1x128 scales
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int r = 8 * warp + i;
+    uint32_t qg = 0, qu = 0;
+    uint2 d2 = make_uint2(0, 0);
+    float sg = 0.0f, su = 0.0f;
+    if (r < nv) {                                // rows past the segment stay zero
       const uint8_t* row = guq + static_cast<long long>(r0 + r) * 2 * f;
-      a = *reinterpret_cast<const uint4*>(row + cb * kTile + v * 16);
-      b = *reinterpret_cast<const uint4*>(row + f + cb * kTile + v * 16);
+      qg = *reinterpret_cast<const uint32_t*>(row + c0);
+      qu = *reinterpret_cast<const uint32_t*>(row + f + c0);
+      d2 = *reinterpret_cast<const uint2*>(dh + static_cast<long long>(r0 + r) * f + c0);
+      sg = sgu[static_cast<long long>(cb) * R + r0 + r];
+      su = sgu[static_cast<long long>(NB + cb) * R + r0 + r];
     }
-    *reinterpret_cast<uint4*>(&tg[r][v * 16]) = a;
-    *reinterpret_cast<uint4*>(&tu[r][v * 16]) = b;
-  }
-  for (int i = tid; i < kTile * 16; i += kBwdThreads) {  // dh: 16 uint4 per row
-    const int r = i >> 4, v = i & 15;
-    uint4 a = make_uint4(0, 0, 0, 0);
-    if (r < nv)
-      a = *reinterpret_cast<const uint4*>(dh + static_cast<long long>(r0 + r) * f + cb * kTile +
-                                          v * 8);
-    *reinterpret_cast<uint4*>(&tdh[r][v * 8]) = a;
-  }
-  if (tid < kTile) {
-    const bool ok = tid < nv;
-    sg_s[tid] = ok ? sgu[static_cast<long long>(cb) * R + r0 + tid] : 0.0f;
-    su_s[tid] = ok ? sgu[static_cast<long long>(NB + cb) * R + r0 + tid] : 0.0f;
-    rmax_g[tid] = 0.0f;
-    rmax_u[tid] = 0.0f;
-  }
-  __syncthreads();
-
-  const int c = tid & (kTile - 1), half = tid >> 7, lane = tid & 31;
-  float cm_h = 0.0f, cm_g = 0.0f, cm_u = 0.0f;
-  for (int r = half * 64; r < half * 64 + 64; ++r) {
-    const SwigluVals v = swiglu_bwd_at(tg[r][c], tu[r][c], sg_s[r], su_s[r],
-                                       bf16_bits_to_f32(tdh[r][c]));
-    cm_h = fmaxf(cm_h, fabsf(v.h));
-    cm_g = fmaxf(cm_g, fabsf(v.dg));
-    cm_u = fmaxf(cm_u, fabsf(v.du));
-    float mg = fabsf(v.dg), mu = fabsf(v.du);
+    float cg[4], cu[4];
+    e4m3x4_decode(qg, cg);
+    e4m3x4_decode(qu, cu);
+    const float dhv[4] = {bf16_bits_to_f32(static_cast<uint16_t>(d2.x & 0xFFFFu)),
+                          bf16_bits_to_f32(static_cast<uint16_t>(d2.x >> 16)),
+                          bf16_bits_to_f32(static_cast<uint16_t>(d2.y & 0xFFFFu)),
+                          bf16_bits_to_f32(static_cast<uint16_t>(d2.y >> 16))};
+    float mg = 0.0f, mu = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const SwigluVals v = swiglu_bwd_at(cg[j], cu[j], sg, su, dhv[j]);
+      hv[i][j] = v.h;
+      gv[i][j] = v.dg;
+      uv[i][j] = v.du;
+      mg = fmaxf(mg, fabsf(v.dg));
+      mu = fmaxf(mu, fabsf(v.du));
+      cm[0][j] = fmaxf(cm[0][j], fabsf(v.h));
+      cm[1][j] = fmaxf(cm[1][j], fabsf(v.dg));
+      cm[2][j] = fmaxf(cm[2][j], fabsf(v.du));
+    }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
       mg = fmaxf(mg, __shfl_xor_sync(0xFFFFFFFFu, mg, off));
       mu = fmaxf(mu, __shfl_xor_sync(0xFFFFFFFFu, mu, off));
     }
-    if (lane == 0) {
-      smem_max(&rmax_g[r], mg);
-      smem_max(&rmax_u[r], mu);
+    const float s_g = e4m3_scale_from_amax(mg), s_u = e4m3_scale_from_amax(mu);
+    rs_g[i] = s_g;
+    rs_u[i] = s_u;
+    if (lane == 0 && r < nv) {
+      sdgu[static_cast<long long>(cb) * R + r0 + r] = s_g;
+      sdgu[static_cast<long long>(NB + cb) * R + r0 + r] = s_u;
     }
   }
-  cpart[0][half][c] = cm_h;
-  cpart[1][half][c] = cm_g;
-  cpart[2][half][c] = cm_u;
+#pragma unroll
+  for (int t = 0; t < 3; ++t)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) cpart[warp][t][4 * lane + j] = cm[t][j];
   __syncthreads();
-
-  // 128x1 scales of this thread's column, 1x128 scales of every row
-  const float s_h = pow2_scale_from_amax(fmaxf(cpart[0][0][c], cpart[0][1][c]));
-  const float s_g = pow2_scale_from_amax(fmaxf(cpart[1][0][c], cpart[1][1][c]));
-  const float s_u = pow2_scale_from_amax(fmaxf(cpart[2][0][c], cpart[2][1][c]));
-  const float rs_h = __frcp_rn(s_h), rs_g = __frcp_rn(s_g), rs_u = __frcp_rn(s_u);
-  const int col = cb * kTile + c;
-  uint32_t wh[16], wg[16], wu[16];
+  if (threadIdx.x < 3 * kTile) {
+    const int t = threadIdx.x / kTile, c = threadIdx.x % kTile;
+    float m = 0.0f;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) { wh[i] = 0; wg[i] = 0; wu[i] = 0; }
+    for (int w = 0; w < 16; ++w) m = fmaxf(m, cpart[w][t][c]);
+    const float sc = pow2_scale_from_amax(m);
+    cscale[t][c] = sc;
+    float* dst = t == 0 ? shT + static_cast<long long>(blockIdx.x) * f
+                        : sdguT + static_cast<long long>(blockIdx.x) * 2 * f + (t - 1) * f;
+    dst[cb * kTile + c] = sc;
+  }
+  __syncthreads();
+  // row-major 1x128 codes of dG and dU (correctly rounded division, the quantiser's rule)
 #pragma unroll
-  for (int j = 0; j < 64; ++j) {
-    const int r = half * 64 + j;
-    const SwigluVals v = swiglu_bwd_at(tg[r][c], tu[r][c], sg_s[r], su_s[r],
-                                       bf16_bits_to_f32(tdh[r][c]));
-    const int sh = 8 * (j & 3);
-    wh[j >> 2] |= e4m3_byte(v.h * rs_h) << sh;
-    wg[j >> 2] |= e4m3_byte(v.dg * rs_g) << sh;
-    wu[j >> 2] |= e4m3_byte(v.du * rs_u) << sh;
-    if (r < nv) {   // the rows' 1x128 codes (FP32-scale rule, correctly rounded division)
-      const float sgr = e4m3_scale_from_amax(rmax_g[r]);
-      const float sur = e4m3_scale_from_amax(rmax_u[r]);
+  for (int i = 0; i < 8; ++i) {
+    const int r = 8 * warp + i;
+    if (r < nv) {
+      uint32_t wg = 0, wu = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        wg |= e4m3_byte(__fdiv_rn(gv[i][j], rs_g[i])) << (8 * j);
+        wu |= e4m3_byte(__fdiv_rn(uv[i][j], rs_u[i])) << (8 * j);
+      }
       uint8_t* out = dguq + static_cast<long long>(r0 + r) * 2 * f;
-      out[col] = static_cast<uint8_t>(e4m3_byte(__fdiv_rn(v.dg, sgr)));
-      out[f + col] = static_cast<uint8_t>(e4m3_byte(__fdiv_rn(v.du, sur)));
+      *reinterpret_cast<uint32_t*>(out + c0) = wg;
+      *reinterpret_cast<uint32_t*>(out + f + c0) = wu;
     }
   }
-  const long long p = static_cast<long long>(blockIdx.x) * kTile + half * 64;
-  uint4* dh_t = reinterpret_cast<uint4*>(hT + static_cast<long long>(col) * ldq + p);
-  uint4* dg_t = reinterpret_cast<uint4*>(dguT + static_cast<long long>(col) * ldq + p);
-  uint4* du_t = reinterpret_cast<uint4*>(dguT + static_cast<long long>(f + col) * ldq + p);
+  // transposed 128x1 codes: 8 rows (bytes) per column and thread; padded rows are 0
+  const long long p = static_cast<long long>(blockIdx.x) * kTile + 8 * warp;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    dh_t[i] = make_uint4(wh[4 * i], wh[4 * i + 1], wh[4 * i + 2], wh[4 * i + 3]);
-    dg_t[i] = make_uint4(wg[4 * i], wg[4 * i + 1], wg[4 * i + 2], wg[4 * i + 3]);
-    du_t[i] = make_uint4(wu[4 * i], wu[4 * i + 1], wu[4 * i + 2], wu[4 * i + 3]);
-  }
-  if (half == 0) {
-    shT[static_cast<long long>(blockIdx.x) * f + col] = s_h;
-    sdguT[static_cast<long long>(blockIdx.x) * 2 * f + col] = s_g;
-    sdguT[static_cast<long long>(blockIdx.x) * 2 * f + f + col] = s_u;
-  }
-  if (tid < kTile && tid < nv) {
-    sdgu[static_cast<long long>(cb) * R + r0 + tid] = e4m3_scale_from_amax(rmax_g[tid]);
-    sdgu[static_cast<long long>(NB + cb) * R + r0 + tid] = e4m3_scale_from_amax(rmax_u[tid]);
+  for (int j = 0; j < 4; ++j) {
+    const int col = c0 + j;
+    const float rh = __frcp_rn(cscale[0][4 * lane + j]);    // exact: powers of two
+    const float rg = __frcp_rn(cscale[1][4 * lane + j]);
+    const float ru = __frcp_rn(cscale[2][4 * lane + j]);
+    uint32_t h0 = 0, h1 = 0, g0 = 0, g1 = 0, u0 = 0, u1 = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      h0 |= e4m3_byte(hv[i][j] * rh) << (8 * i);
+      h1 |= e4m3_byte(hv[i + 4][j] * rh) << (8 * i);
+      g0 |= e4m3_byte(gv[i][j] * rg) << (8 * i);
+      g1 |= e4m3_byte(gv[i + 4][j] * rg) << (8 * i);
+      u0 |= e4m3_byte(uv[i][j] * ru) << (8 * i);
+      u1 |= e4m3_byte(uv[i + 4][j] * ru) << (8 * i);
+    }
+    *reinterpret_cast<uint2*>(hT + static_cast<long long>(col) * ldq + p) = make_uint2(h0, h1);
+    *reinterpret_cast<uint2*>(dguT + static_cast<long long>(col) * ldq + p) = make_uint2(g0, g1);
+    *reinterpret_cast<uint2*>(dguT + static_cast<long long>(f + col) * ldq + p) = make_uint2(u0, u1);
   }
 }
 
@@ -416,10 +425,7 @@ int launch_swiglu_bwd(const uint8_t* guq, const float* sgu, const uint16_t* dh, 
                       const int32_t* seg, const int32_t* pad, int G, int max_blocks, int ldq,
                       uint8_t* dguq, float* sdgu, uint8_t* hT, float* shT, uint8_t* dguT,
                       float* sdguT, cudaStream_t stream) {
-  constexpr int smem = 2 * kTile * (kTile + 16) + kTile * (kTile + 8) * 2;
-  if (set_max_dynamic_smem(reinterpret_cast<const void*>(swiglu_bwd_kernel), smem) != MOE_OK)
-    return MOE_ERR_CUDA;
-  swiglu_bwd_kernel<<<dim3(max_blocks, f / kTile), kBwdThreads, smem, stream>>>(
+  swiglu_bwd_kernel<<<dim3(max_blocks, f / kTile), kSwThreads, 0, stream>>>(
       guq, sgu, dh, R, f, seg, pad, G, ldq, dguq, sdgu, hT, shT, dguT, sdguT);
   return check_launch();
 }
