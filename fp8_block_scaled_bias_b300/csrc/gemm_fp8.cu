@@ -778,7 +778,7 @@ int launch_fp8_gemm(const GemmArgs& a, GemmEpilogue epi, cudaStream_t stream) {
   // segments of a few rows (decode batches): weight rows on the MMA's M side
   const bool swap_ok = a.N % 256 == 0 && epi != kEpiSwiGLUCache;
   if (swap_ok && (mode == 3 || (mode == 0 && static_cast<long long>(a.M) <= 16LL * a.G)))
-    return launch_fp8_gemm_swap(a, epi, stream);
+    return launch_fp8_gemm_swap(a, epi, false, stream);
   const bool pair = mode == 2;
   return pair ? launch_tiling<true>(a, epi, p, stream) : launch_tiling<false>(a, epi, p, stream);
 }

@@ -683,6 +683,16 @@ int launch_mx_gemm(const uint8_t* A, const float* sA, const uint8_t* B, const fl
                    cudaStream_t stream) {
   if (M == 0) return MOE_OK;
   if (N % 128 != 0 || (epi == kEpiSwiGLU && N % 256 != 0)) return MOE_ERR_UNSUPPORTED;
+  // Segments of a few rows (decode batches): the swapped-operand kernel, whose software
+  // promotion with power-of-two scales is exact, like the tensor core's block scaling.
+  const int mode = gemm_tiling();
+  if (N % 256 == 0 && (mode == 3 || (mode == 0 && static_cast<long long>(M) <= 16LL * G))) {
+    GemmArgs a{};
+    a.A = A; a.sA = sA; a.B = B; a.sB = sB; a.seg = seg;
+    a.G = G; a.M = M; a.N = N; a.K = K; a.C = C; a.ldc = ldc; a.hq = hq; a.sh = sh;
+    a.status = status;
+    return launch_fp8_gemm_swap(a, epi, true, stream);
+  }
   MxParams p;
   p.sA = sA; p.sB = sB; p.seg = seg;
   p.G = G; p.M = M; p.N = N; p.K = K;

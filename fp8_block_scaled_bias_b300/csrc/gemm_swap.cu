@@ -28,6 +28,12 @@
 // of 128 hidden columns, so the up threads pass their values to the gate threads through
 // shared memory, h = silu(gate) * up, and each token's 1x128 scale is the max over the
 // tile's 128 hidden columns.
+//
+// POW2: the MX-native recipe's short segments.  Its scales are powers of two, so each
+// promotion product sB * sA * partial is exact -- the scaling the tensor core's block
+// scales would apply -- and h is requantised with the power-of-two rule.  A scale that is
+// not a positive normal power of two is reported as MOE_ERR_DEVICE_DATA, as the MX
+// kernel does.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -112,9 +118,14 @@ MOE_DEV void drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
 
 MOE_DEV float silu_swap(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
+MOE_DEV bool is_pow2_scale(float s) {
+  const uint32_t b = __float_as_uint(s), e = (b >> 23) & 0xFFu;
+  return (b & 0x807FFFFFu) == 0 && e != 0 && e != 0xFFu;
+}
+
 }  // namespace
 
-template <int EPI>
+template <int EPI, bool POW2>
 __global__ void __launch_bounds__(sw::THREADS, 1)
     fp8_gemm_swap_kernel(const __grid_constant__ CUtensorMap tmA,
                          const __grid_constant__ CUtensorMap tmB, const SwapParams p) {
@@ -312,7 +323,7 @@ __global__ void __launch_bounds__(sw::THREADS, 1)
     float* xch = reinterpret_cast<float*>(smem + OFF_XCH);
     float* amx = reinterpret_cast<float*>(smem + OFF_AMAX);
     uint32_t it = 0;
-    bool ok = true;
+    bool ok = true, badscale = false;
     for (int unit = first_unit; ok && unit < total; unit += unit_stride) {
       int g, r0, wb;
       swap_unit(unit, ustart, seg, G, NWB, g, r0, wb);
@@ -335,6 +346,8 @@ __global__ void __launch_bounds__(sw::THREADS, 1)
         // interleave a half holds 64 gate rows (gate block, slot 0) and the matching 64 up
         // rows (up block, slot 1)
         const float swt = sl[TOK + (EPI == kEpiSwiGLU ? (q >> 1) : h)];
+        if (POW2 && warp == 2)                      // one warp checks the slot's scales
+          badscale |= !is_pow2_scale(sl[lane]) || (lane < 2 && !is_pow2_scale(sl[TOK + lane]));
         float2 sc2[TOK / 2];
 #pragma unroll
         for (int i = 0; i < TOK / 4; ++i) {       // token scales x the weight scale
@@ -398,8 +411,8 @@ __global__ void __launch_bounds__(sw::THREADS, 1)
 #pragma unroll
           for (int c = 0; c < TOK; ++c) {
             const float amax = fmaxf(fmaxf(amx[c], amx[TOK + c]), fmaxf(amx[2 * TOK + c], amx[3 * TOK + c]));
-            const float s = e4m3_scale_from_amax(amax);
-            const float rs = __frcp_rn(s);
+            const float s = POW2 ? pow2_scale_from_amax(amax) : e4m3_scale_from_amax(amax);
+            const float rs = __frcp_rn(s);                 // exact when s is a power of two
             if (c < nv) {
               hrow[static_cast<long long>(c) * f] =
                   static_cast<uint8_t>(f32x2_to_e4m3x2(__fmul_rn(hv[c], rs), 0.0f) & 0xFFu);
@@ -410,6 +423,8 @@ __global__ void __launch_bounds__(sw::THREADS, 1)
         named_bar_sync_or(EPI_BAR, EPI_WARPS * 32, false);   // xch / amx free again
       }
     }
+    if (POW2 && __any_sync(0xFFFFFFFFu, badscale) && lane == 0)
+      set_status(p.status, MOE_ERR_DEVICE_DATA);
   }
 
   tc_fence_before();
@@ -426,7 +441,7 @@ bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* ptr
                     uint64_t inner, uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
                     uint32_t box_outer);   // runtime.cu
 
-int launch_fp8_gemm_swap(const GemmArgs& a, GemmEpilogue epi, cudaStream_t stream) {
+int launch_fp8_gemm_swap(const GemmArgs& a, GemmEpilogue epi, bool pow2, cudaStream_t stream) {
   using namespace sw;
   if (a.M == 0) return MOE_OK;
   if (a.N % WROWS != 0 || (epi != kEpiBF16 && epi != kEpiSwiGLU)) return MOE_ERR_UNSUPPORTED;
@@ -445,17 +460,17 @@ int launch_fp8_gemm_swap(const GemmArgs& a, GemmEpilogue epi, cudaStream_t strea
   long long grid = num_sms();
   if (units < grid) grid = units;
   if (grid < 1) grid = 1;
-  const void* fn = epi == kEpiSwiGLU
-                       ? reinterpret_cast<const void*>(fp8_gemm_swap_kernel<kEpiSwiGLU>)
-                       : reinterpret_cast<const void*>(fp8_gemm_swap_kernel<kEpiBF16>);
-  if (set_max_dynamic_smem(fn, SMEM_ALLOC) != MOE_OK) return MOE_ERR_CUDA;
+  auto run = [&](auto kern) {
+    if (set_max_dynamic_smem(reinterpret_cast<const void*>(kern), SMEM_ALLOC) != MOE_OK)
+      return MOE_ERR_CUDA;
+    kern<<<static_cast<unsigned>(grid), THREADS, SMEM_ALLOC, stream>>>(tmA, tmB, p);
+    return check_launch();
+  };
   if (epi == kEpiSwiGLU)
-    fp8_gemm_swap_kernel<kEpiSwiGLU>
-        <<<static_cast<unsigned>(grid), THREADS, SMEM_ALLOC, stream>>>(tmA, tmB, p);
-  else
-    fp8_gemm_swap_kernel<kEpiBF16>
-        <<<static_cast<unsigned>(grid), THREADS, SMEM_ALLOC, stream>>>(tmA, tmB, p);
-  return check_launch();
+    return pow2 ? run(fp8_gemm_swap_kernel<kEpiSwiGLU, true>)
+                : run(fp8_gemm_swap_kernel<kEpiSwiGLU, false>);
+  return pow2 ? run(fp8_gemm_swap_kernel<kEpiBF16, true>)
+              : run(fp8_gemm_swap_kernel<kEpiBF16, false>);
 }
 
 }  // namespace moe

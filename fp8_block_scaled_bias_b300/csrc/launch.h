@@ -89,8 +89,9 @@ struct GemmArgs {
 };
 int launch_fp8_gemm(const GemmArgs& a, GemmEpilogue epi, cudaStream_t stream);
 // Grouped GEMM for short segments with the operands swapped (gemm_swap.cu): weight rows on
-// the MMA's M side, 32 tokens on N.  BF16 and SwiGLU epilogues; N % 256 == 0.
-int launch_fp8_gemm_swap(const GemmArgs& a, GemmEpilogue epi, cudaStream_t stream);
+// the MMA's M side, 32 tokens on N.  BF16 and SwiGLU epilogues; N % 256 == 0.  pow2: h is
+// requantised with the power-of-two rule (the MX-native recipe's short segments).
+int launch_fp8_gemm_swap(const GemmArgs& a, GemmEpilogue epi, bool pow2, cudaStream_t stream);
 // CTA tiling of the grouped GEMM: 0 automatic, 1 one CTA per 128-row tile, 2 CTA pairs
 // per 256-row tile (tcgen05 cta_group::2), 3 swapped operands for short segments.
 // Process-wide.

@@ -250,7 +250,10 @@ int moe_test_gemm_wait_expiry(const uint8_t* A, const float* sA, const uint8_t* 
  * (tcgen05.mma kind::mxf8f6f4, UE8M0 scale factors) and one FP32 accumulator per tile
  * for the whole K loop: no per-block promotion.  Scales must be positive normal powers
  * of two (fp8_quant_*_pow2); anything else sets MOE_ERR_DEVICE_DATA.  Same layouts and
- * limits as fp8_blockscaled_grouped_gemm; no workspace. */
+ * limits as fp8_blockscaled_grouped_gemm; no workspace.  Segments of a few rows (decode
+ * batches: M <= 16 * G, N % 256 == 0, see moe_set_gemm_tiling) run on the swapped-operand
+ * kernel instead, whose per-block promotion with power-of-two scales is exact -- the same
+ * scaling the tensor core would apply. */
 int fp8_mx_grouped_gemm(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
                         const int32_t* seg_offsets, int G, int M, int N, int K, uint16_t* C,
                         int ldc, int32_t* dev_status, void* stream);

@@ -333,10 +333,13 @@ def test_tiny_mx_layer_from_identical_logits():
     assert_close(bf16_to_f32(layer.y), ref["y"], what="layer output (MX)")
 
 
-def test_v3_mx_layer_sampled_tokens():
+def test_v3_and_decode_mx_layer_sampled_tokens():
+    """The MX-native layer at the V3 shape (the block-scaled tensor-core GEMMs) and on the
+    decode batch (short segments: the swapped-operand kernel with power-of-two scales)."""
     w = make_weights(workloads.V3, DEV, pow2=True)
     try:
         _check_config(workloads.V3, w, n_sample=16, mx=True)
+        _check_config(workloads.DECODE, w, n_sample=16, mx=True)
     finally:
         del w
         torch.cuda.empty_cache()

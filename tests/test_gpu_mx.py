@@ -1,6 +1,8 @@
 """GPU parity of the MX-native variant (power-of-two scales applied by the tensor core,
 tcgen05.mma kind::mxf8f6f4) against the oracle: the power-of-two quantisers bit-exact,
-the GEMM against the exact block-scaled definition."""
+the GEMM against the exact block-scaled definition.  Short segments (decode batches) take
+the swapped-operand kernel, whose power-of-two promotion is exact; both paths are
+covered."""
 
 import numpy as np
 import pytest
@@ -97,6 +99,25 @@ def test_grouped_ragged_mx_gemm_paired_tile(N):
     sB = _pow2_scales((G, N // 128, K // 128), 63)
     C = _run(A, sA, B, sB, seg, M)
     assert_close(C, _ref(A, sA, B, sB, seg), what=f"mx grouped paired N={N}")
+
+
+def test_mx_short_segments_on_swapped_operands():
+    """Decode-like segments (M <= 16 G, N % 256 == 0) take the swapped-operand kernel with
+    exact power-of-two promotion; against the oracle."""
+    rng = np.random.default_rng(23)
+    counts = rng.integers(0, 9, 40)
+    counts[[1, 5]] = 0
+    counts[[8, 9]] = [1, 37]
+    seg = np.concatenate([[0], np.cumsum(counts)]).tolist()
+    G, N, K = len(counts), 512, 384
+    M = seg[-1]
+    assert M <= 16 * G
+    A = workloads.gen_fp8_codes(M, K, sub_seed=81)
+    B = torch.stack([workloads.gen_fp8_codes(N, K, sub_seed=90 + g) for g in range(G)])
+    sA = _pow2_scales((K // 128, M), 82)
+    sB = _pow2_scales((G, N // 128, K // 128), 83)
+    C = _run(A, sA, B, sB, seg, M)
+    assert_close(C, _ref(A, sA, B, sB, seg), what="mx short segments")
 
 
 def test_pow2_quantisers_bit_exact():
