@@ -226,3 +226,19 @@ def test_router_logits_additive_in_x():
     x2 = rng.integers(-4, 5, (3, d)).astype(np.float32)
     assert np.array_equal(oracle.router_logits(x1 + x2, cen),
                           oracle.router_logits(x1, cen) + oracle.router_logits(x2, cen))
+
+
+def test_route_scale_multiplies_gates_only():
+    """The release config's routed scaling factor ([book] ch. 3 and ch. 7: 2.5) multiplies
+    the normalised gates and nothing else: the same experts in the same order, and every
+    gate equal to fl32(2.5 * the unscaled gate), so the gates sum to 2.5 (within the
+    float32 rounding of K products)."""
+    rng = np.random.default_rng(12)
+    T, E, G, M, K = 64, 32, 8, 4, 8
+    s = rng.uniform(0, 1, (T, E)).astype(np.float32)
+    b = rng.uniform(-0.01, 0.01, E).astype(np.float32)
+    i1, g1 = oracle.route(s, b, G, M, K // M, K, scores_are_affinities=True)
+    i25, g25 = oracle.route(s, b, G, M, K // M, K, route_scale=2.5, scores_are_affinities=True)
+    assert np.array_equal(i1, i25)
+    assert np.array_equal(g25, (g1 * np.float32(2.5)).astype(np.float32))
+    assert np.allclose(g25.astype(np.float64).sum(1), 2.5, atol=K * 2.5 * 2.0 ** -23)
