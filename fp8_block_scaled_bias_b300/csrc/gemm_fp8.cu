@@ -38,9 +38,9 @@
 //   warps 2..9  promotion + epilogue: warp w reads TMEM lanes 32*(w%4).. (its rows);
 //               warps 2-5 own 128 of the 256 columns, warps 6-9 the other 128.  Each
 //               thread adds its partials into 128 FP32 accumulators with packed FMAs,
-//               16 columns per TMEM load; the scales arrive through per-thread cp.async
-//               rings SPF K blocks ahead (measured faster on this B300 than a separate
-//               feeder warp with an mbarrier-tracked ring).
+//               16 columns per TMEM load; each K block's scales are loaded from global
+//               memory into registers during the K block before (measured faster on
+//               this B300 than cp.async rings in shared memory or a feeder warp).
 // The tile list walks segments in order, then N tiles, with the M tiles of a segment
 // fastest so CTAs working at the same time share the expert's weight tile through L2.
 // Segments need not be multiples of the tile height: rows past a segment's end are
@@ -76,7 +76,6 @@ constexpr int EPI_THREADS = EPI_WARPS * 32;
 constexpr int SCHED_WARP = 2 + EPI_WARPS;          // waits on barriers for the MMA warp
 constexpr int THREADS = 64 + EPI_THREADS + 32;
 constexpr int MMA_BAR = 1;                         // named barrier: MMA warp + scheduler
-constexpr int SPF = 8;                             // K blocks of scales prefetched ahead
 constexpr int MAX_G = 1024;
 constexpr int TBUF = 2;                            // TMEM partial buffers of BN columns
 constexpr uint32_t TMEM_COLS = 512;
@@ -98,10 +97,7 @@ struct Layout {
   static constexpr int OFF_TSTART = OFF_SEG + (MAX_G + 1) * 4;
   // row max-abs exchange: [2 bufs][h, gate, up][2 column halves][128 rows]
   static constexpr int OFF_AMAX = OFF_TSTART + (MAX_G + 1) * 4;
-  // per-thread rings of prefetched scales: sA [SPF][EPI_THREADS], sB [SPF][EPI_WARPS][2]
-  static constexpr int OFF_SCALE_A = OFF_AMAX + 2 * 3 * 2 * ROWS * 4;
-  static constexpr int OFF_SCALE_B = OFF_SCALE_A + SPF * EPI_THREADS * 4;
-  static constexpr int SMEM_USED = OFF_SCALE_B + SPF * EPI_WARPS * 2 * 4;
+  static constexpr int SMEM_USED = OFF_AMAX + 2 * 3 * 2 * ROWS * 4;
   static constexpr int SMEM_ALLOC = SMEM_USED + 1024;              // 1024-B alignment slack
   static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 };
@@ -449,7 +445,6 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
     const int q = warp & 3;             // TMEM lane window
     const int row = q * 32 + lane;      // row within this CTA's 128 rows
     const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
-    const int etid = tid - 64;
     const int NB = p.N / 128;           // weight-scale rows per segment
     // the arrival that releases a TMEM buffer goes to the MMA-issuing CTA
     const uint32_t tempty_dst[TBUF] = {PAIR ? mapa_shared(tempty_bar(0), 0) : tempty_bar(0),
@@ -459,49 +454,26 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
     auto col_of = [](int c) {
       return static_cast<uint32_t>((SWIGLU) ? (c < 4 ? 0 : 64) + (c & 3) * 16 : c * 16);
     };
-    // Scale prefetch: every K block needs sA[kb][row] (this thread's row) and the one or
-    // two weight scales of the tile's N blocks.  They are copied into shared-memory rings
-    // SPF K blocks ahead with cp.async, following the same (unit, K block) sequence as
-    // the promotion loop, so the L2 latency never sits on the critical path.
-    const uint32_t ring_a = sbase + L::OFF_SCALE_A + static_cast<uint32_t>(etid) * 4;
-    const uint32_t ring_b = sbase + L::OFF_SCALE_B + static_cast<uint32_t>(warp - 2) * 8;
-    const float* ring_a_f = reinterpret_cast<const float*>(smem + L::OFF_SCALE_A) + etid;
-    const float* ring_b_f = reinterpret_cast<const float*>(smem + L::OFF_SCALE_B) + (warp - 2) * 2;
-    int pf_unit = first_unit, pf_kb = 0;                 // prefetch cursor
-    int pf_g = 0, pf_m0 = 0, pf_nt = 0;
-    bool pf_live = pf_unit < total;
-    if (pf_live) decode_unit<BM>(pf_unit, ustart, seg, G, pf_g, pf_m0, pf_nt);
-    uint32_t pf_it = 0;
-    auto prefetch_one = [&]() {
-      // issue the copies of the cursor's K block into ring slot pf_it % SPF, then advance
-      if (pf_live) {
-        // (a half-filled last tile has no second N block: read a valid scale, unused)
-        const int nb0 = (SWIGLU) ? 2 * pf_nt : min(2 * pf_nt + grp, NB - 1);
-        const int nb1 = (SWIGLU) ? 2 * pf_nt + 1 : nb0;
-        const int slot = static_cast<int>(pf_it % SPF);
-        const int arow = min(pf_m0 + row_off + row, p.M - 1);
-        cp_async_4(ring_a + slot * EPI_THREADS * 4,
-                   p.sA + static_cast<long long>(pf_kb) * p.M + arow);
-        if (lane == 0) {
-          const float* sb = p.sB + static_cast<long long>(pf_g) * NB * KB + pf_kb;
-          cp_async_4(ring_b + slot * EPI_WARPS * 8, sb + static_cast<long long>(nb0) * KB);
-          cp_async_4(ring_b + slot * EPI_WARPS * 8 + 4, sb + static_cast<long long>(nb1) * KB);
-        }
-        if (++pf_kb == KB) {
-          pf_kb = 0;
-          pf_unit += unit_stride;
-          pf_live = pf_unit < total;
-          if (pf_live) decode_unit<BM>(pf_unit, ustart, seg, G, pf_g, pf_m0, pf_nt);
-        }
-      }
-      cp_async_commit();                                 // one group per K block, maybe empty
-      ++pf_it;
+    // Scales: every K block needs sA[kb][row] (this thread's row) and the one or two
+    // weight scales of the tile's N blocks.  They are loaded from global memory into
+    // registers one K block ahead: the loads for K block it + 1 are issued before the wait
+    // for K block it, so a K block of waiting and folding covers most of their latency.
+    // (The weight scales are the same address in every lane: one broadcast load.)
+    auto load_scales = [&](int g_, int m0_, int nt_, int kb_, float& a, float& b0, float& b1) {
+      const int nb0 = (SWIGLU) ? 2 * nt_ : min(2 * nt_ + grp, NB - 1);
+      const int nb1 = (SWIGLU) ? 2 * nt_ + 1 : nb0;
+      const int arow = min(m0_ + row_off + row, p.M - 1);
+      a = __ldg(p.sA + static_cast<long long>(kb_) * p.M + arow);
+      const float* sb = p.sB + static_cast<long long>(g_) * NB * KB + kb_;
+      b0 = __ldg(sb + static_cast<long long>(nb0) * KB);
+      b1 = __ldg(sb + static_cast<long long>(nb1) * KB);
     };
-    for (int i = 0; i < SPF - 1; ++i) prefetch_one();
-    // the scales of the first K block, read one block ahead from then on
-    cp_async_wait<SPF - 2>();
-    __syncwarp();
-    float nsa = ring_a_f[0], nsb0 = ring_b_f[0], nsb1 = ring_b_f[1];
+    float csa = 1.0f, csb0 = 1.0f, csb1 = 1.0f;          // scales of the current K block
+    if (first_unit < total) {
+      int g, m0, nt;
+      decode_unit<BM>(first_unit, ustart, seg, G, g, m0, nt);
+      load_scales(g, m0, nt, 0, csa, csb0, csb1);
+    }
 
     uint32_t it = 0;
     uint32_t xch = 0;                                    // row max-abs exchanges so far
@@ -515,7 +487,14 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
 #pragma unroll
       for (int i = 0; i < 64; ++i) acc2[i] = make_float2(0.0f, 0.0f);
       for (int kb = 0; kb < KB; ++kb, ++it) {
-        const float sa = nsa, sb0 = nsb0, sb1 = nsb1;
+        float nsa = 1.0f, nsb0 = 1.0f, nsb1 = 1.0f;
+        if (kb + 1 < KB) {
+          load_scales(g, m0, nt, kb + 1, nsa, nsb0, nsb1);
+        } else if (unit + unit_stride < total) {         // the next unit's first K block
+          int ng, nm0, nnt;
+          decode_unit<BM>(unit + unit_stride, ustart, seg, G, ng, nm0, nnt);
+          load_scales(ng, nm0, nnt, 0, nsa, nsb0, nsb1);
+        }
         const int b = it % TBUF;
         const uint32_t bph = (it / TBUF) & 1;
         if (!mbar_wait_warp<PAIR>(tfull_bar(b), bph, abort_flag, p.status, wait_ns)) {
@@ -523,8 +502,8 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
           break;
         }
         tc_fence_after();
-        const float sc0 = __fmul_rn(sa, sb0);
-        const float sc1 = __fmul_rn(sa, sb1);
+        const float sc0 = __fmul_rn(csa, csb0);
+        const float sc1 = __fmul_rn(csa, csb1);
         const uint32_t tb = tmem_base + lane_addr + static_cast<uint32_t>(b * BN + grp * 128);
         // two 16-column loads in flight per wait: four TMEM round trips per K block
 #pragma unroll
@@ -550,30 +529,38 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
           if (PAIR) mbar_arrive_cluster(tempty_dst[b]);
           else mbar_arrive(tempty_dst[b]);
         }
-        // scales of K block it + 1: their shared-memory latency overlaps the next wait
-        prefetch_one();                                  // K block it + SPF - 1
-        cp_async_wait<SPF - 2>();                        // this thread's copies for it + 1
-        __syncwarp();                                    // lane 0's weight scales too
-        const int nslot = static_cast<int>((it + 1) % SPF);
-        nsa = ring_a_f[nslot * EPI_THREADS];
-        nsb0 = ring_b_f[nslot * EPI_WARPS * 2];
-        nsb1 = ring_b_f[nslot * EPI_WARPS * 2 + 1];
+        csa = nsa;
+        csb0 = nsb0;
+        csb1 = nsb1;
       }
       if (!ok) break;
       float* acc = reinterpret_cast<float*>(acc2);
 
       if (EPI == kEpiBF16) {
         if (row < rv && nt * BN + grp * 128 < p.N) {
-          uint4* dst = reinterpret_cast<uint4*>(p.C + static_cast<long long>(r0 + row) * p.ldc +
-                                                nt * BN + grp * 128);
+          uint16_t* crow = p.C + static_cast<long long>(r0 + row) * p.ldc + nt * BN + grp * 128;
+          // a row's 128 values leave as 32-byte stores when C and its row pitch allow
+          // (a warp's store instruction covers 32 rows, one sector each), else 16-byte
+          if (((reinterpret_cast<uintptr_t>(p.C) | static_cast<uintptr_t>(p.ldc) * 2) & 31) == 0) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            uint4 o;
-            o.x = pack_bf16x2(acc[8 * j + 0], acc[8 * j + 1]);
-            o.y = pack_bf16x2(acc[8 * j + 2], acc[8 * j + 3]);
-            o.z = pack_bf16x2(acc[8 * j + 4], acc[8 * j + 5]);
-            o.w = pack_bf16x2(acc[8 * j + 6], acc[8 * j + 7]);
-            dst[j] = o;
+            for (int j = 0; j < 8; ++j) {
+              const float* v = acc + 16 * j;
+              st_global_v8(crow + 16 * j, pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                           pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]),
+                           pack_bf16x2(v[8], v[9]), pack_bf16x2(v[10], v[11]),
+                           pack_bf16x2(v[12], v[13]), pack_bf16x2(v[14], v[15]));
+            }
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(crow);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              uint4 o;
+              o.x = pack_bf16x2(acc[8 * j + 0], acc[8 * j + 1]);
+              o.y = pack_bf16x2(acc[8 * j + 2], acc[8 * j + 3]);
+              o.z = pack_bf16x2(acc[8 * j + 4], acc[8 * j + 5]);
+              o.w = pack_bf16x2(acc[8 * j + 6], acc[8 * j + 7]);
+              dst[j] = o;
+            }
           }
         }
       } else {
@@ -648,7 +635,6 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
         }
       }
     }
-    cp_async_wait<0>();                                  // no copy may land after exit
   }
 
   tc_fence_before();

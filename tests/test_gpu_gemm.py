@@ -117,6 +117,29 @@ def test_grouped_with_gathered_rows(tiling):
     _check(C, _ref(A, sA, B, sB, seg, a_rows), "gathered")
 
 
+def test_grouped_strided_output(tiling):
+    """C as a column window of a wider buffer: a row pitch and base that are 16- but not
+    32-byte aligned (the epilogue's 16-byte store path); the columns around it stay."""
+    counts = [70, 0, 200, 33]
+    seg = np.concatenate([[0], np.cumsum(counts)]).tolist()
+    M, N, K, G = seg[-1], 384, 384, len(counts)
+    A = _codes(M, K, 41)
+    sA = workloads.gen_scales((K // 128, M), sub_seed=42)
+    B = _codes(G * N, K, 43).view(G, N, K)
+    sB = workloads.gen_scales((G, N // 128, K // 128), sub_seed=44)
+    buf = torch.full((M, N + 24), 7.0, dtype=torch.bfloat16, device=DEV)
+    C = buf[:, 8:8 + N]
+    assert (C.stride(0) * 2) % 32 == 16 and C.data_ptr() % 32 == 16
+    st = ops.new_status(DEV)
+    ops.grouped_gemm(A.to(DEV), sA.to(DEV), B.to(DEV), sB.to(DEV),
+                     torch.tensor(seg, dtype=torch.int32, device=DEV), M, status=st, out=C)
+    torch.cuda.synchronize()
+    assert ops.status_value(st) == 0
+    full = bf16_to_f32(buf)
+    assert (full[:, :8] == 7.0).all() and (full[:, 8 + N:] == 7.0).all()
+    _check(full[:, 8:8 + N], _ref(A, sA, B, sB, seg), "strided C")
+
+
 def test_bad_segment_table_is_reported(tiling):
     A = torch.zeros(64, 128, dtype=torch.uint8, device=DEV)
     sA = torch.ones(1, 64, device=DEV)

@@ -164,7 +164,8 @@ def test_route_affinities_bit_exact(cfg, T):
 
 
 def test_route_other_shapes_and_route_scale():
-    for (E, G, M, K, n) in [(64, 8, 3, 6, 2), (32, 1, 1, 5, 5), (1024, 32, 4, 32, 8), (48, 4, 4, 4, 3)]:
+    for (E, G, M, K, n) in [(64, 8, 3, 6, 2), (32, 1, 1, 5, 5), (1024, 32, 4, 32, 8), (48, 4, 4, 4, 3),
+                           (512, 16, 4, 8, 2), (288, 9, 3, 8, 2)]:
         rng = np.random.default_rng(E + K)
         s = rng.uniform(0, 1, (300, E)).astype(np.float32)
         b = rng.uniform(-0.05, 0.05, E).astype(np.float32)
