@@ -26,15 +26,10 @@
 // Warp roles:
 //   warp 0      TMA producer of this CTA's A and B rows, STAGES-deep ring.  In the pair
 //               tiling both CTAs' loads complete on the first CTA's stage barrier.
-//   warp 1      TMEM allocation; one thread issues 4 MMAs (K32 each) per K block into
-//               TMEM buffer (kb mod 2) and commits to the stage and buffer barriers (of
-//               both CTAs in the pair tiling; only the first CTA issues).  This warp
-//               never touches shared memory in its loop: on this tensor core a shared-
-//               memory access by the issuing warp (an mbarrier wait included) waits
-//               behind the operand reads of its MMAs in flight and leaves the pipe idle.
-//   warp 10     MMA scheduler: waits on the stage and TMEM-buffer mbarriers for each K
-//               block and releases warp 1 through a named barrier (lockstep; its OR-
-//               reduction carries an abort, so both warps leave the loop together)
+//   warp 1      TMEM allocation; one thread waits for the stage and for TMEM buffer
+//               (kb mod 2), issues 4 MMAs (K32 each) per K block into that buffer and
+//               commits to the stage and buffer barriers (of both CTAs in the pair
+//               tiling; only the first CTA issues).
 //   warps 2..9  promotion + epilogue: warp w reads TMEM lanes 32*(w%4).. (its rows);
 //               warps 2-5 own 128 of the 256 columns, warps 6-9 the other 128.  Each
 //               thread adds its partials into 128 FP32 accumulators with packed FMAs,
@@ -73,9 +68,7 @@ constexpr int ROWS = 128;                          // accumulator rows per CTA (
 constexpr int A_BYTES = ROWS * BK;
 constexpr int EPI_WARPS = 8;
 constexpr int EPI_THREADS = EPI_WARPS * 32;
-constexpr int SCHED_WARP = 2 + EPI_WARPS;          // waits on barriers for the MMA warp
-constexpr int THREADS = 64 + EPI_THREADS + 32;
-constexpr int MMA_BAR = 1;                         // named barrier: MMA warp + scheduler
+constexpr int THREADS = 64 + EPI_THREADS;
 constexpr int MAX_G = 1024;
 constexpr int TBUF = 2;                            // TMEM partial buffers of BN columns
 constexpr uint32_t TMEM_COLS = 512;
@@ -116,7 +109,7 @@ struct GemmParams {
   float* sgu;            // and their 1x128 scales [N/128][M]
   int32_t* status;
   uint64_t wait_ns;      // limit of every mbarrier wait
-  int stall;             // != 0: the scheduler waits on a barrier nothing arrives on
+  int stall;             // != 0: the MMA issuer waits on a barrier nothing arrives on
 };
 
 namespace {
@@ -375,70 +368,52 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
       }
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer (no shared-memory access in the loop) ----------------
-    if (issuer) {
+    // ---------------- MMA issuer ----------------
+    // One thread waits for stage s (full) and TMEM buffer b (released by the promotion
+    // warps), then issues the K block's four MMAs and the commits.  Waiting here directly
+    // takes a hop out of the buffer round trip that sets the pace: a separate waiting
+    // warp releasing this one through a named barrier measured ~450 cycles slower per
+    // round trip on this B300.
+    if (issuer && lane == 0) {
       constexpr uint32_t idesc = make_idesc(BM, BN, 0u, 0u);   // E4M3 x E4M3 -> F32
       uint32_t it = 0;
       bool ok = true;
       for (int unit = first_unit; ok && unit < total; unit += unit_stride) {
         for (int kb = 0; kb < KB; ++kb, ++it) {
-          // released by the scheduler once stage s is full and TMEM buffer b is free
-          if (named_bar_sync_or(MMA_BAR, 64, false)) { ok = false; break; }
-          if (lane == 0) {
-            const int s = it % STAGES;
-            const int b = it % TBUF;
-            tc_fence_after();
-            const uint64_t adesc = smem_desc_sw128(sbase + L::OFF_A + s * A_BYTES);
-            const uint64_t bdesc = smem_desc_sw128(sbase + L::OFF_B + s * L::B_BYTES);
-            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
-#pragma unroll
-            for (int k = 0; k < BK / 32; ++k)   // K = 32 bytes per MMA: +2 in the >>4 address
-              mma_fp8_g<PAIR>(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, k > 0 ? 1u : 0u);
-            if (PAIR) {
-              mma_commit_g<true>(mapa_shared(empty_bar(s), 0));
-              mma_commit_g<true>(mapa_shared(empty_bar(s), 1));
-              mma_commit_g<true>(mapa_shared(tfull_bar(b), 0));
-              mma_commit_g<true>(mapa_shared(tfull_bar(b), 1));
-            } else {
-              mma_commit(empty_bar(s));
-              mma_commit(tfull_bar(b));
-            }
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          const int b = it % TBUF;
+          const uint32_t bph = (it / TBUF) & 1;
+          // (failure-path test: a barrier nothing arrives on)
+          if (!((!p.stall || mbar_wait(stall_bar, 0, abort_flag, p.status, wait_ns)) &&
+                mbar_wait<PAIR>(full_bar(s), ph, abort_flag, p.status, wait_ns) &&
+                mbar_wait<PAIR>(tempty_bar(b), bph ^ 1, abort_flag, p.status, wait_ns))) {
+            ok = false;
+            break;
           }
-          __syncwarp();
+          tc_fence_after();
+          const uint64_t adesc = smem_desc_sw128(sbase + L::OFF_A + s * A_BYTES);
+          const uint64_t bdesc = smem_desc_sw128(sbase + L::OFF_B + s * L::B_BYTES);
+          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
+#pragma unroll
+          for (int k = 0; k < BK / 32; ++k)   // K = 32 bytes per MMA: +2 in the >>4 address
+            mma_fp8_g<PAIR>(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, k > 0 ? 1u : 0u);
+          if (PAIR) {
+            mma_commit_g<true>(mapa_shared(empty_bar(s), 0));
+            mma_commit_g<true>(mapa_shared(empty_bar(s), 1));
+            mma_commit_g<true>(mapa_shared(tfull_bar(b), 0));
+            mma_commit_g<true>(mapa_shared(tfull_bar(b), 1));
+          } else {
+            mma_commit(empty_bar(s));
+            mma_commit(tfull_bar(b));
+          }
         }
       }
       // every MMA issued so far must finish before TMEM is released
-      if (lane == 0) {
-        mma_commit_g<PAIR>(drain_bar);
-        mbar_drain(drain_bar, 0, wait_ns);
-      }
-      __syncwarp();
+      mma_commit_g<PAIR>(drain_bar);
+      mbar_drain(drain_bar, 0, wait_ns);
     }
-  } else if (warp == SCHED_WARP) {
-    // ---------------- MMA scheduler ----------------
-    // Same iteration sequence as the MMA warp; one named barrier per K block.
-    if (issuer) {
-      uint32_t it = 0;
-      bool ok = true;
-      for (int unit = first_unit; ok && unit < total; unit += unit_stride) {
-        for (int kb = 0; kb < KB; ++kb, ++it) {
-          int good = 1;
-          if (lane == 0) {
-            const int s = it % STAGES;
-            const uint32_t ph = (it / STAGES) & 1;
-            const int b = it % TBUF;
-            const uint32_t bph = (it / TBUF) & 1;
-            // failure-path test: a barrier nothing arrives on
-            good = (!p.stall || mbar_wait(stall_bar, 0, abort_flag, p.status, wait_ns)) &&
-                   mbar_wait<PAIR>(tempty_bar(b), bph ^ 1, abort_flag, p.status, wait_ns) &&
-                   mbar_wait<PAIR>(full_bar(s), ph, abort_flag, p.status, wait_ns);
-          }
-          good = __shfl_sync(0xFFFFFFFFu, good, 0);
-          tc_fence_before();
-          if (named_bar_sync_or(MMA_BAR, 64, good == 0)) { ok = false; break; }
-        }
-      }
-    }
+    __syncwarp();
   } else if (warp >= 2 && warp < 2 + EPI_WARPS) {
     // ---------------- promotion + epilogue ----------------
     const int grp = (warp - 2) >> 2;    // column half of the tile

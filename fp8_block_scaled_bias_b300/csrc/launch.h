@@ -85,7 +85,7 @@ struct GemmArgs {
   float* sgu;            // and their 1x128 scales [N/128][M]
   int32_t* status;
   uint64_t wait_ns;      // 0: the default limit of every mbarrier wait
-  int stall;             // failure-path test: the scheduler waits on a barrier nothing arrives on
+  int stall;             // failure-path test: the MMA issuer waits on a barrier nothing arrives on
 };
 int launch_fp8_gemm(const GemmArgs& a, GemmEpilogue epi, cudaStream_t stream);
 // Grouped GEMM for short segments with the operands swapped (gemm_swap.cu): weight rows on

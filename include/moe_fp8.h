@@ -235,7 +235,7 @@ int moe_get_gemm_tiling(void);
 
 /* Failure-path test of the kernels' bounded waits; not for production use.  Runs
  * fp8_blockscaled_grouped_gemm (a_rows = NULL, same arguments) with every mbarrier wait
- * limited to wait_ns nanoseconds (1e5 <= wait_ns <= 2e9) and the MMA scheduler first
+ * limited to wait_ns nanoseconds (1e5 <= wait_ns <= 2e9) and the MMA-issuing thread first
  * waiting on a barrier that nothing arrives on.  That wait expires: the kernel writes
  * MOE_ERR_DEVICE_TIMEOUT to dev_status (required), stops issuing work, lets its copies
  * and tensor-core operations in flight finish, frees its TMEM and returns, leaving C

@@ -4,7 +4,7 @@ last N tile, gathered A rows, and the five full-size sweep shapes on sampled row
 small cases run under every tiling (one CTA per 128-row tile; CTA pairs sharing one
 cta_group::2 MMA per 256-row tile; swapped operands with weight rows on the MMA's M side,
 which falls back to the first when N % 256 != 0).  The failure path of the bounded waits is exercised
-by a launch whose scheduler waits on a barrier nothing arrives on."""
+by a launch whose MMA-issuing thread waits on a barrier nothing arrives on."""
 
 import numpy as np
 import pytest
@@ -256,7 +256,7 @@ def test_swapped_tiling_short_segments(lib):
 
 @pytest.mark.parametrize("mode", [1, 2], ids=["single", "pair"])
 def test_bounded_wait_expiry_reports_and_recovers(lib, mode):
-    """Failure detection without a GPU fault: the scheduler waits on a barrier nothing
+    """Failure detection without a GPU fault: the MMA issuer waits on a barrier nothing
     arrives on, with every wait limited to 1 ms.  The kernel must report
     MOE_ERR_DEVICE_TIMEOUT, drain, free its TMEM and return within milliseconds, and the
     next (normal) launch on the same GPU must be correct."""
