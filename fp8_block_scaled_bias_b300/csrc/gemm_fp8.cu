@@ -480,17 +480,18 @@ __global__ void __launch_bounds__(gk::THREADS, 1)
         const float sc0 = __fmul_rn(csa, csb0);
         const float sc1 = __fmul_rn(csa, csb1);
         const uint32_t tb = tmem_base + lane_addr + static_cast<uint32_t>(b * BN + grp * 128);
-        // two 16-column loads in flight per wait: four TMEM round trips per K block
+        // four 16-column loads in flight per wait: two TMEM round trips per K block
+        // (chunks 0-3 take the first N block's scale, 4-7 the second's)
 #pragma unroll
-        for (int c = 0; c < 8; c += 2) {
-          uint32_t v[2][16];
-          tmem_ld_32x32b_x16(tb + col_of(c), v[0]);
-          tmem_ld_32x32b_x16(tb + col_of(c + 1), v[1]);
+        for (int c = 0; c < 8; c += 4) {
+          uint32_t v[4][16];
+#pragma unroll
+          for (int h = 0; h < 4; ++h) tmem_ld_32x32b_x16(tb + col_of(c + h), v[h]);
           const float sc = (c < 4) ? sc0 : sc1;
           const float2 sc2 = make_float2(sc, sc);
           tmem_ld_wait();
 #pragma unroll
-          for (int h = 0; h < 2; ++h)
+          for (int h = 0; h < 4; ++h)
 #pragma unroll
             for (int i = 0; i < 8; ++i)
               acc2[(c + h) * 8 + i] = __ffma2_rn(
@@ -731,16 +732,16 @@ int launch_fp8_gemm(const GemmArgs& a, GemmEpilogue epi, cudaStream_t stream) {
   p.guq = a.guq; p.sgu = a.sgu;
   p.wait_ns = a.wait_ns ? a.wait_ns : kWaitLimitNs;
   p.stall = a.stall;
-  // Automatic choice: the pair tiling for dense-sized segments (>= 4096 rows on average),
-  // where halving each CTA's B bytes makes it 2-6% faster on this B300; the single tiling
-  // for MoE segments, where 256-row tiles compute more padding rows than they save (the
-  // skewed 16384-token layer: single 10.7 ms vs pair 11.7 ms for gate/up).
+  // Automatic choice: the single tiling.  With the buffer round trip bound by the
+  // promotion's TMEM reads, the pair tiling's smaller B loads buy nothing and its
+  // cross-CTA release costs time: measured on this B300, single beats pair on the five
+  // dense sweep shapes (by 2-15%) and on the skewed MoE layer.  The pair stays selectable.
   const int mode = g_tiling.load();
   // segments of a few rows (decode batches): weight rows on the MMA's M side
   const bool swap_ok = a.N % 256 == 0 && epi != kEpiSwiGLUCache;
   if (swap_ok && (mode == 3 || (mode == 0 && static_cast<long long>(a.M) <= 16LL * a.G)))
     return launch_fp8_gemm_swap(a, epi, false, stream);
-  const bool pair = mode == 2 || (mode == 0 && static_cast<long long>(a.M) >= 4096LL * a.G);
+  const bool pair = mode == 2;
   return pair ? launch_tiling<true>(a, epi, p, stream) : launch_tiling<false>(a, epi, p, stream);
 }
 

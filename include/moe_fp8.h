@@ -218,9 +218,8 @@ size_t fp8_grouped_gemm_ws_bytes(int M, int K, int has_a_rows);
 /* CTA tiling of fp8_blockscaled_grouped_gemm, moe_gate_up_fp8 and moe_swiglu_fp8_fwd
  * (a performance choice; results are the same bits either way):
  *   0  automatic (the default): tiling 3 when the segments average at most 16 rows
- *      (M <= 16 * G, decode batches) and N % 256 == 0; tiling 2 when they average at
- *      least 4096 rows (dense-sized GEMMs, where it measured 2-6% faster on B300);
- *      else tiling 1 (MoE segments, where 256-row tiles add more padding than they save);
+ *      (M <= 16 * G, decode batches) and N % 256 == 0, else tiling 1 (on B300 tiling 2
+ *      measured 2-15% slower on dense shapes and slower on MoE segments);
  *   1  one CTA per 128-row x 256-column tile (tcgen05 cta_group::1);
  *   2  two CTAs of a cluster per 256-row x 256-column tile: one tcgen05 cta_group::2
  *      MMA over both CTAs' shared memory, each CTA loading half of the weight tile;
