@@ -2,7 +2,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--config v3|decode|skewed|tiny|v3_e32|sweep|sweep_mx] [--mx]
-                    [--backward] [--tiling auto|single|pair]
+                    [--backward] [--tiling auto|single|pair|swap]
 
 One step is one pass of the whole hot path over one batch: router logits, routing,
 permutation, 1x128 quantisation, row gather, gate/up grouped GEMM with fused SwiGLU and
@@ -61,7 +61,7 @@ def parse():
                          "the tensor core) instead of FP32 scales with software promotion")
     ap.add_argument("--backward", action="store_true",
                     help="layer configs: time a training step (forward + expert backward)")
-    ap.add_argument("--tiling", choices=["auto", "single", "pair"], default="auto",
+    ap.add_argument("--tiling", choices=["auto", "single", "pair", "swap"], default="auto",
                     help="CTA tiling of the FP32-scale grouped GEMM (moe_set_gemm_tiling)")
     ap.add_argument("--shape", default=None,
                     help="sweep configs only: one M,N,K instead of the five sweep shapes")
@@ -677,7 +677,7 @@ def main_reference(args, cfg, rank, world, dev):
 
 def _lib_tiling():
     from fp8_block_scaled_bias_b300 import load
-    return {0: "auto", 1: "single", 2: "pair"}[load().moe_get_gemm_tiling()]
+    return {0: "auto", 1: "single", 2: "pair", 3: "swap"}[load().moe_get_gemm_tiling()]
 
 
 def main_sweep(args, rank, dev, mx=False):
@@ -759,7 +759,7 @@ def main():
         from fp8_block_scaled_bias_b300.build import build
         build()
     lib = pkg.load()
-    lib.moe_set_gemm_tiling({"auto": 0, "single": 1, "pair": 2}[args.tiling])
+    lib.moe_set_gemm_tiling({"auto": 0, "single": 1, "pair": 2, "swap": 3}[args.tiling])
     if args.config in ("sweep", "sweep_mx"):
         main_sweep(args, rank, dev, mx=args.config == "sweep_mx")
     elif args.backward:
