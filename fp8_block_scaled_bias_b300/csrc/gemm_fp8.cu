@@ -20,9 +20,10 @@
 //           the first CTA's shared memory and A rows [128, 256), B rows [128, 256) from
 //           the second's, and writes rows [0, 128) of the accumulator into the first
 //           CTA's TMEM and rows [128, 256) into the second's.  Each CTA loads 32 KB per K
-//           block for the same MMA work per SM, so a third fewer bytes ride the L2 ->
-//           shared-memory path that bounds the single tiling.  Each CTA still promotes
-//           its own 128 rows.
+//           block for the same MMA work per SM (a third fewer bytes through L2), and still
+//           promotes its own 128 rows.  The pace of both tilings is the TMEM buffer round
+//           trip (promotion reads, MMA, barrier latencies), which the pair lengthens with
+//           its cross-CTA release: measured slower than the single tiling on B300.
 // Warp roles:
 //   warp 0      TMA producer of this CTA's A and B rows, STAGES-deep ring.  In the pair
 //               tiling both CTAs' loads complete on the first CTA's stage barrier.
