@@ -51,9 +51,10 @@ int moe_router_logits(const uint16_t* x, int T, int d, const uint16_t* w_hilo, i
   if (T < 0 || d <= 0 || E <= 0 || d % 128 != 0 || E % 16 != 0) return MOE_ERR_INVALID_ARG;
   if (E > 256) return MOE_ERR_UNSUPPORTED;
   if (T == 0) return MOE_OK;
-  if (!x || !w_hilo || !z || !aligned16(x) || !aligned16(w_hilo)) return MOE_ERR_INVALID_ARG;
+  if (!x || !w_hilo || !z || !aligned16(x) || !aligned16(w_hilo) || !aligned16(z))
+    return MOE_ERR_INVALID_ARG;
   const size_t need = moe::router_logits_ws_bytes(T, d, E);
-  if (need > 0 && (!ws || ws_bytes < need)) return MOE_ERR_WORKSPACE;
+  if (need > 0 && (!ws || ws_bytes < need || !aligned16(ws))) return MOE_ERR_WORKSPACE;
   return moe::launch_router_logits(x, T, d, w_hilo, E, z, dev_status, ws, as_stream(stream));
 }
 

@@ -6,8 +6,11 @@
 // bits); x is BF16, so every product hi*x and lo*x is exact and both planes accumulate
 // into one FP32 TMEM accumulator: z = sum_k x_k hi_k + x_k lo_k.
 //
-// One CTA per 128-token x BN-expert tile (BN = min(64, E)); the whole K = d loop runs in
-// the CTA with a 6-stage TMA pipeline (x tile 128x64 BF16, hi and lo tiles BNx64).
+// One CTA per 128-token x BN-expert tile (BN = min(64, E)) and K range, with a 6-stage TMA
+// pipeline (x tile 128x64 BF16, hi and lo tiles BNx64).  When there are fewer tiles than
+// SMs (decode batches: T = 128 gives 4 tiles) the K loop is split across CTAs
+// (blockIdx.z) into FP32 partial tiles in the workspace, summed afterwards in split order
+// by a second kernel, so the result does not depend on timing.
 //   warp 0      TMA producer
 //   warp 1      TMEM allocation; one thread issues 8 MMAs (M128 N=BN K16) per 64-deep
 //               K block: 4 K steps on the hi plane and 4 on the lo plane
@@ -38,6 +41,8 @@ struct RouterParams {
   float* z;
   int T, d, E, BN;
   int32_t* status;
+  float* part;           // split K: [splits][T][E] partial sums (else NULL: write z)
+  int kb_per;            // K blocks per split
 };
 
 __global__ void __launch_bounds__(rk::THREADS, 1)
@@ -60,8 +65,10 @@ __global__ void __launch_bounds__(rk::THREADS, 1)
   const int BN = p.BN;
   const int m0 = blockIdx.y * BM;
   const int n0 = blockIdx.x * BN;
-  const int KB = p.d / BK;
+  const int kb0 = static_cast<int>(blockIdx.z) * p.kb_per;   // this CTA's K range
+  const int KB = min(p.d / BK - kb0, p.kb_per);
   const uint32_t stage_tx = A_BYTES + 2u * BN * BK * 2;
+  float* const out = p.part ? p.part + static_cast<long long>(blockIdx.z) * p.T * p.E : p.z;
 
   if (tid == 0) {
     *abort_flag = 0;
@@ -88,9 +95,10 @@ __global__ void __launch_bounds__(rk::THREADS, 1)
         if (!mbar_wait(empty_bar(s), ph ^ 1, abort_flag, p.status)) { ok = false; break; }
         const uint32_t st = sbase + s * STAGE_BYTES;
         mbar_arrive_expect_tx(full_bar(s), stage_tx);
-        tma_load_2d(st, &tmX, kb * BK, m0, full_bar(s));
-        tma_load_2d(st + A_BYTES, &tmW, kb * BK, n0, full_bar(s));              // hi plane
-        tma_load_2d(st + A_BYTES + B_BYTES, &tmW, kb * BK, p.E + n0, full_bar(s));  // lo plane
+        const int kx = (kb0 + kb) * BK;
+        tma_load_2d(st, &tmX, kx, m0, full_bar(s));
+        tma_load_2d(st + A_BYTES, &tmW, kx, n0, full_bar(s));              // hi plane
+        tma_load_2d(st + A_BYTES + B_BYTES, &tmW, kx, p.E + n0, full_bar(s));  // lo plane
       }
       if (!ok) {
         const int first = kb > STAGES ? kb - STAGES : 0;
@@ -139,7 +147,7 @@ __global__ void __launch_bounds__(rk::THREADS, 1)
           tmem_ld_32x32b_x32(tb + c, v);
           tmem_ld_wait();
           if (t < p.T) {
-            float4* dst = reinterpret_cast<float4*>(p.z + static_cast<long long>(t) * p.E + n0 + c);
+            float4* dst = reinterpret_cast<float4*>(out + static_cast<long long>(t) * p.E + n0 + c);
 #pragma unroll
             for (int j = 0; j < 8; ++j)
               dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
@@ -150,7 +158,7 @@ __global__ void __launch_bounds__(rk::THREADS, 1)
           tmem_ld_32x32b_x32(tb + c, v);     // columns c..c+31 lie inside the 64 allocated
           tmem_ld_wait();
           if (t < p.T) {
-            float4* dst = reinterpret_cast<float4*>(p.z + static_cast<long long>(t) * p.E + n0 + c);
+            float4* dst = reinterpret_cast<float4*>(out + static_cast<long long>(t) * p.E + n0 + c);
 #pragma unroll
             for (int j = 0; j < 4; ++j)
               dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
@@ -173,32 +181,82 @@ bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* ptr
                     uint64_t inner, uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
                     uint32_t box_outer);   // runtime.cu
 
+namespace {
+// widest multiple of 16 <= 64 dividing E
+int router_bn(int E) {
+  for (int b = rk::MAX_BN; b >= 16; b -= 16)
+    if (E % b == 0) return b;
+  return 16;
+}
+
+// K splits for T tokens: enough CTAs to cover the SMs, at least 4 K blocks per split.
+// Returns the number of splits (1: no split) and the K blocks per split.
+int router_splits(int T, int d, int E, int* kb_per) {
+  const int KB = d / rk::BK;
+  const long long tiles = static_cast<long long>(E / router_bn(E)) * ((T + rk::BM - 1) / rk::BM);
+  long long S = tiles > 0 ? num_sms() / tiles : 1;
+  if (S > KB / 4) S = KB / 4;
+  if (S < 2) { *kb_per = KB; return 1; }
+  const int per = static_cast<int>((KB + S - 1) / S);
+  *kb_per = per;
+  return (KB + per - 1) / per;
+}
+
+// z = sum of the split partials, added in split order
+__global__ void router_reduce_kernel(const float4* __restrict__ part, int S, long long n4,
+                                     float4* __restrict__ z) {
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n4;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    float4 a = part[i];
+    for (int s = 1; s < S; ++s) {
+      const float4 b = part[static_cast<long long>(s) * n4 + i];
+      a.x = __fadd_rn(a.x, b.x);
+      a.y = __fadd_rn(a.y, b.y);
+      a.z = __fadd_rn(a.z, b.z);
+      a.w = __fadd_rn(a.w, b.w);
+    }
+    z[i] = a;
+  }
+}
+}  // namespace
+
 size_t router_logits_ws_bytes(int T, int d, int E) {
-  (void)T; (void)d; (void)E;
-  return 0;
+  if (T <= 0 || d <= 0 || E <= 0) return 0;
+  int per = 0;
+  const int S = router_splits(T, d, E, &per);
+  return S > 1 ? static_cast<size_t>(S) * T * E * sizeof(float) : 0;
 }
 
 int launch_router_logits(const uint16_t* x, int T, int d, const uint16_t* w_hilo, int E,
                          float* z, int32_t* status, void* ws, cudaStream_t stream) {
   using namespace rk;
-  (void)ws;
   if (T == 0) return MOE_OK;
-  int BN = 16;                                   // widest multiple of 16 <= 64 dividing E
-  for (int b = MAX_BN; b >= 16; b -= 16)
-    if (E % b == 0) { BN = b; break; }
+  const int BN = router_bn(E);
   if (E % BN != 0) return MOE_ERR_UNSUPPORTED;
+  int kb_per = 0;
+  const int S = router_splits(T, d, E, &kb_per);
+  if (S > 1 && !ws) return MOE_ERR_WORKSPACE;
   CUtensorMap tmX, tmW;
   if (!encode_tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, d, T, 2ull * d, BK, BM))
     return MOE_ERR_CUDA;
   if (!encode_tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w_hilo, d, 2ull * E, 2ull * d, BK,
                       BN))
     return MOE_ERR_CUDA;
-  RouterParams p{z, T, d, E, BN, status};
+  RouterParams p{z, T, d, E, BN, status, S > 1 ? static_cast<float*>(ws) : nullptr, kb_per};
   if (set_max_dynamic_smem(reinterpret_cast<const void*>(router_logits_kernel), SMEM_ALLOC) !=
       MOE_OK)
     return MOE_ERR_CUDA;
-  dim3 grid(E / BN, (T + BM - 1) / BM);
+  dim3 grid(E / BN, (T + BM - 1) / BM, S);
   router_logits_kernel<<<grid, THREADS, SMEM_ALLOC, stream>>>(tmX, tmW, p);
+  if (S > 1) {
+    const int st = check_launch();
+    if (st != MOE_OK) return st;
+    const long long n4 = static_cast<long long>(T) * E / 4;
+    long long blocks = (n4 + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    router_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        static_cast<const float4*>(ws), S, n4, reinterpret_cast<float4*>(z));
+  }
   return check_launch();
 }
 

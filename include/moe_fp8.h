@@ -79,8 +79,11 @@ int moe_version(void);
  * (moe_router_split_bf16), so the products run on BF16 tensor cores with FP32
  * accumulation and E keeps 16 significant bits.
  * Limits: d % 128 == 0, E % 16 == 0, E <= 256, T >= 0; x and w_hilo 16-byte aligned.
- * ws: moe_router_logits_ws_bytes (currently 0).  z: FP32 [T][E].  A bounded wait that
- * expires inside the kernel sets MOE_ERR_DEVICE_TIMEOUT in dev_status (may be NULL). */
+ * ws: moe_router_logits_ws_bytes(T, d, E) bytes, 16-byte aligned: nonzero when there are
+ * fewer 128-token tiles than SMs (e.g. T = 128), where the K loop is split across CTAs into
+ * FP32 partials that a second launch sums in a fixed order (the same bits every call).
+ * z: FP32 [T][E], 16-byte aligned.  A bounded wait that expires inside the kernel sets
+ * MOE_ERR_DEVICE_TIMEOUT in dev_status (may be NULL). */
 int moe_router_logits(const uint16_t* x, int T, int d, const uint16_t* w_hilo, int E,
                       float* z, int32_t* dev_status, void* ws, size_t ws_bytes, void* stream);
 size_t moe_router_logits_ws_bytes(int T, int d, int E);

@@ -345,10 +345,12 @@ def test_combine_reports_bad_row():
 # ---- router logits -------------------------------------------------------------------
 
 @pytest.mark.parametrize("T,d,E", [(1, 128, 16), (130, 512, 16), (256, 512, 48), (300, 384, 80),
-                                   (4096, 7168, 256)])
+                                   (128, 7168, 256), (4096, 7168, 256)])
 def test_router_logits_against_oracle(T, d, E):
     """z on BF16 tensor cores from the hi/lo split: within 2^-14 of sum_k |x_k e_k| of the
-    exact product (dropping the lo plane would miss by about 2^-9 of it)."""
+    exact product (dropping the lo plane would miss by about 2^-9 of it).  The small-T
+    shapes run with the K loop split across CTAs (partials summed in split order), and
+    the split result must repeat bit for bit."""
     g = torch.Generator().manual_seed(T + d + E)
     x = torch.randn(T, d, generator=g)
     x[:, :4] *= 30.0                                   # outlier channels
@@ -364,6 +366,8 @@ def test_router_logits_against_oracle(T, d, E):
     assert (np.abs(z - z_ref) <= bound).all()
     assert np.array_equal(oracle.router_logits(x.float().numpy(), cen.numpy()),
                           z_ref.astype(np.float32))
+    z2 = ops.router_logits(x.to(DEV), hilo, st).cpu().numpy()
+    assert np.array_equal(z, z2)
 
 
 def test_router_split_planes():
