@@ -16,7 +16,9 @@ constexpr int kCombineThreads = 128;
 constexpr int kMaxK = 32;
 }  // namespace
 
-// One block per token; each thread owns 8 consecutive columns at a time.
+// One block per token (SLICED: per token and column slice, blockIdx.y); each thread owns
+// 8 consecutive columns at a time.
+template <bool SLICED>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
     const uint16_t* __restrict__ y_rows, int n_rows, const int32_t* __restrict__ row_of,
     const float* __restrict__ gate, int K, int d, int shared_row_base,
@@ -41,7 +43,10 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
   __syncthreads();
   if (bad) return;
   const int nv = d / 8;
-  for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+  const int v0 = SLICED ? static_cast<int>(blockIdx.y * blockDim.x + threadIdx.x)
+                        : static_cast<int>(threadIdx.x);
+  const int vstep = SLICED ? static_cast<int>(gridDim.y * blockDim.x) : static_cast<int>(blockDim.x);
+  for (int v = v0; v < nv; v += vstep) {
     float acc[8];
     if (shared_row_base >= 0) {
       const uint4 u = __ldcs(reinterpret_cast<const uint4*>(y_rows + rows[kMaxK]) + v);
@@ -79,8 +84,18 @@ int launch_combine(const uint16_t* y_rows, int n_rows, const int32_t* row_of,
                    const float* gate, int T, int K, int d, int shared_row_base, uint16_t* y,
                    int32_t* status, cudaStream_t stream) {
   if (T == 0) return MOE_OK;
-  combine_kernel<<<T, kCombineThreads, 0, stream>>>(y_rows, n_rows, row_of, gate, K, d,
-                                                     shared_row_base, y, status);
+  // Decode-sized batches: a token's row is split over several blocks (up to one 8-column
+  // vector per thread) until the grid fills the SMs, so a thread's K + 1 row loads are
+  // most of the latency (T = 128: 25 -> 12 us).  Large batches keep one block per token.
+  const int max_slices = (d / 8 + kCombineThreads - 1) / kCombineThreads;
+  const long long want = (static_cast<long long>(num_sms()) * 16 + T - 1) / T;
+  const int slices = static_cast<int>(want < 1 ? 1 : (want > max_slices ? max_slices : want));
+  if (slices > 1)
+    combine_kernel<true><<<dim3(T, slices), kCombineThreads, 0, stream>>>(
+        y_rows, n_rows, row_of, gate, K, d, shared_row_base, y, status);
+  else
+    combine_kernel<false><<<T, kCombineThreads, 0, stream>>>(y_rows, n_rows, row_of, gate, K, d,
+                                                            shared_row_base, y, status);
   return check_launch();
 }
 

@@ -159,10 +159,93 @@ __global__ void __launch_bounds__(kPermThreads) permute_scatter_kernel(
   }
 }
 
+// A single chunk (T <= kChunkTokens, decode batches): the three passes in one block --
+// per-warp histograms, the exclusive scan over experts (segment offsets), per-warp bases,
+// then the same ordered hand-out as permute_scatter_kernel.  One launch instead of three.
+__global__ void __launch_bounds__(kPermThreads) permute_single_kernel(
+    const int32_t* __restrict__ idx, int T, int K, int E, int include_shared,
+    int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ row_token,
+    int32_t* __restrict__ row_of, int32_t* status) {
+  extern __shared__ int32_t next_row[];        // [kPermWarps][E]
+  __shared__ int warp_tot[kPermWarps];
+  const int np = T * K;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int run = ((np + kPermWarps - 1) / kPermWarps + 31) & ~31;
+  const int p_begin = min(np, warp * run), p_end = min(np, p_begin + run);
+  for (int i = threadIdx.x; i < kPermWarps * E; i += blockDim.x) next_row[i] = 0;
+  __syncthreads();
+  for (int p = p_begin + lane; p < p_end; p += 32) {
+    const int e = idx[p];
+    if (e < 0 || e >= E) set_status(status, MOE_ERR_DEVICE_DATA);
+    else atomicAdd(&next_row[warp * E + e], 1);   // counts: order-free
+  }
+  __syncthreads();
+  // exclusive scan of the expert totals: thread i owns experts [i*per, i*per + per)
+  const int per = (E + kPermThreads - 1) / kPermThreads;
+  const int e0 = min(E, static_cast<int>(threadIdx.x) * per), e1 = min(E, e0 + per);
+  int local = 0;
+  for (int e = e0; e < e1; ++e)
+    for (int w = 0; w < kPermWarps; ++w) local += next_row[w * E + e];
+  int incl = local;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  int base = incl - local;
+  for (int w = 0; w < warp; ++w) base += warp_tot[w];
+  __syncthreads();                             // every thread has read the totals
+  for (int e = e0; e < e1; ++e) {
+    int row = base, n = 0;
+    for (int w = 0; w < kPermWarps; ++w) {
+      const int c = next_row[w * E + e];
+      next_row[w * E + e] = row;               // this warp's first row in segment e
+      row += c;
+      n += c;
+    }
+    counts[e] = n;
+    offsets[e] = base;
+    base += n;
+  }
+  if (threadIdx.x == 0) {
+    offsets[E] = T * K;
+    offsets[E + 1] = T * K + (include_shared ? T : 0);
+  }
+  __syncthreads();
+  int32_t* mine = next_row + warp * E;
+  const unsigned lt = (1u << lane) - 1u;
+  for (int b0 = p_begin; b0 < p_end; b0 += 32) {
+    const int p = b0 + lane;
+    int e = p < p_end ? idx[p] : -1;
+    const bool valid = e >= 0 && e < E;
+    if (!valid) e = -1 - lane;                 // a key no other lane holds
+    const unsigned same = __match_any_sync(0xFFFFFFFFu, e);
+    if (valid) {
+      const int row = mine[e] + __popc(same & lt);
+      row_of[p] = row;
+      row_token[row] = p / K;
+    }
+    __syncwarp();
+    if (valid && lane == 31 - __clz(same)) mine[e] += __popc(same);
+    __syncwarp();
+  }
+  if (include_shared)
+    for (int i = threadIdx.x; i < T; i += blockDim.x) row_token[static_cast<long long>(T) * K + i] = i;
+}
+
 int launch_permute(const int32_t* idx, int T, int K, int E, int include_shared,
                    int32_t* counts, int32_t* offsets, int32_t* row_token, int32_t* row_of,
                    int32_t* status, void* ws, cudaStream_t stream) {
   const int nc = n_chunks(T);
+  if (nc == 1) {
+    const size_t smem = static_cast<size_t>(kPermWarps) * E * sizeof(int32_t);
+    permute_single_kernel<<<1, kPermThreads, smem, stream>>>(idx, T, K, E, include_shared,
+                                                            counts, offsets, row_token, row_of,
+                                                            status);
+    return check_launch() == MOE_OK ? MOE_OK : MOE_ERR_CUDA;
+  }
   int32_t* chunk = static_cast<int32_t*>(ws);
   if (nc > 0) {
     permute_count_kernel<<<nc, kPermThreads, E * sizeof(int32_t), stream>>>(idx, T, K, E, chunk,
