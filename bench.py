@@ -503,8 +503,7 @@ def main_ours(args, cfg, rank, world, dev):
     gu_ms = st["gate_up"] / fw
     fp8_peak, peak_note = fp8_peak_for(pk, r["clocks"])
     gemm_ms = (st["gate_up"] + st["down"]) / fw
-    roof = kernel_roofline("fp8_mx_gemm_kernel<SwiGLU> (gate/up grouped GEMM)" if args.mx else
-                           "fp8_gemm_kernel<SwiGLU> (gate/up grouped GEMM)", gu_bytes,
+    roof = kernel_roofline(gate_up_kernel_name(cfg, T, args.mx, _lib_tiling()), gu_bytes,
                            gate_up_flops(cfg, T), gu_ms, pk, fp8_peak)
     roof["traffic"] = committed_traffic() if cfg.name == "v3" and not args.mx else None
     roof["peak_source"] = pk["source"] + (f" ({peak_note})" if roof["bound"] == "tensor"
@@ -673,6 +672,17 @@ def main_reference(args, cfg, rank, world, dev):
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(out), flush=True)
+
+
+def gate_up_kernel_name(cfg, T, mx, tiling):
+    """The kernel that runs the gate/up GEMM: segments averaging at most 16 rows (decode
+    batches) go to the swapped-operand kernel, in either scale recipe."""
+    rows, G = T * cfg.K + T, cfg.E + 1
+    if tiling == "swap" or (tiling == "auto" and rows <= 16 * G):
+        return "fp8_gemm_swap_kernel<SwiGLU> (gate/up grouped GEMM, weight rows on the MMA M side)"
+    if mx:
+        return "fp8_mx_gemm_kernel<SwiGLU> (gate/up grouped GEMM)"
+    return "fp8_gemm_kernel<SwiGLU> (gate/up grouped GEMM)"
 
 
 def _lib_tiling():

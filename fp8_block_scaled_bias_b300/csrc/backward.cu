@@ -252,13 +252,41 @@ MOE_DEV SwigluVals swiglu_bwd_at(float dg_code, float du_code, float sg, float s
 
 }  // namespace
 
-// Block (rb, cb): the segment rows of padded block rb, hidden columns [128 cb, 128 cb + 128),
-// 512 threads.  Warp w owns rows 8 w .. 8 w + 7, lane l columns 4 l .. 4 l + 3, so every
-// value is computed once and kept in registers: the rows' 1x128 max-abs of dG and dU come
-// from a warp reduction per row, the columns' 128x1 max-abs of h, dG and dU from a
-// shared-memory reduction over the 16 warps.  Loads and the row-major stores are
-// coalesced; the transposed codes go out as 8 contiguous bytes per column and thread.
+// One tile is (rb, cb): the segment rows of padded block rb, hidden columns
+// [128 cb, 128 cb + 128).  512 threads; warp w owns rows 8 w .. 8 w + 7, lane l columns
+// 4 l .. 4 l + 3, so every value is computed once and kept in registers: the rows' 1x128
+// max-abs of dG and dU come from a warp reduction per row, the columns' 128x1 max-abs of
+// h, dG and dU from a shared-memory reduction over the 16 warps.  The row-major stores
+// are coalesced; the transposed codes go out as 8 contiguous bytes per column and thread.
+//
+// The kernel is persistent (one block per SM, the register file holds one tile's values)
+// and streams its tiles through two shared-memory input buffers: the next tile's g, u, dh
+// rows and scales are copied in with cp.async while the current one is computed, so the
+// loads of a whole tile are in flight together instead of one row of them at a time.
 constexpr int kSwThreads = 512;
+
+struct SwTile {                          // one tile's inputs; rows past the segment are 0
+  uint8_t g[kTile * kTile];              // gate codes [row][column]
+  uint8_t u[kTile * kTile];              // up codes
+  uint16_t dh[kTile * kTile];            // dh (BF16)
+  float sg[kTile], su[kTile];            // the rows' 1x128 scales of g and u
+};
+constexpr int kSwSmem = 2 * static_cast<int>(sizeof(SwTile));
+
+namespace {
+// 16- and 4-byte asynchronous copies; a copy with valid == false reads nothing and writes
+// zeros (the source operand is then only a placeholder inside the tensor).
+MOE_DEV void cp_async_16z(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+MOE_DEV void cp_async_4z(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src),
+               "r"(valid ? 4 : 0)
+               : "memory");
+}
+}  // namespace
 
 __global__ void __launch_bounds__(kSwThreads, 1) swiglu_bwd_kernel(
     const uint8_t* __restrict__ guq, const float* __restrict__ sgu,
@@ -266,118 +294,167 @@ __global__ void __launch_bounds__(kSwThreads, 1) swiglu_bwd_kernel(
     const int32_t* __restrict__ pad, int G, int ldq, uint8_t* __restrict__ dguq,
     float* __restrict__ sdgu, uint8_t* __restrict__ hT, float* __restrict__ shT,
     uint8_t* __restrict__ dguT, float* __restrict__ sdguT) {
+  extern __shared__ __align__(16) uint8_t sw_smem[];
   __shared__ float cpart[16][3][kTile];          // per-warp column max: h, dG, dU
   __shared__ float cscale[3][kTile];             // the columns' power-of-two scales
-  int e, r0, nv;
-  if (!block_of(seg, pad, G, blockIdx.x, e, r0, nv)) return;
-  const int cb = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  SwTile* const buf = reinterpret_cast<SwTile*>(sw_smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NB = f / kTile;
-  const int c0 = cb * kTile + 4 * lane;          // this lane's first hidden column
-  float hv[8][4], gv[8][4], uv[8][4];            // h, dG, dU of the warp's 8 rows
-  float cm[3][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-  float rs_g[8], rs_u[8];                        // the rows' 1x128 scales
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int r = 8 * warp + i;
-    uint32_t qg = 0, qu = 0;
-    uint2 d2 = make_uint2(0, 0);
-    float sg = 0.0f, su = 0.0f;
-    if (r < nv) {                                // rows past the segment stay zero
-      const uint8_t* row = guq + static_cast<long long>(r0 + r) * 2 * f;
-      qg = *reinterpret_cast<const uint32_t*>(row + c0);
-      qu = *reinterpret_cast<const uint32_t*>(row + f + c0);
-      d2 = *reinterpret_cast<const uint2*>(dh + static_cast<long long>(r0 + r) * f + c0);
-      sg = sgu[static_cast<long long>(cb) * R + r0 + r];
-      su = sgu[static_cast<long long>(NB + cb) * R + r0 + r];
+  const int ntiles = pad[G] / kTile * NB;
+
+  // tile t -> (padded row block rb, column block cb, segment rows r0 .. r0 + nv - 1)
+  auto tile_of = [&](int t, int& rb, int& cb, int& r0, int& nv) {
+    rb = t / NB;
+    cb = t - rb * NB;
+    int e;
+    block_of(seg, pad, G, rb, e, r0, nv);
+  };
+  auto load_tile = [&](SwTile* in, int r0, int nv, int cb) {
+    for (int i = threadIdx.x; i < kTile * 8; i += kSwThreads) {      // g and u: 8 x 16 B a row
+      const int r = i >> 3, c = i & 7;
+      const bool v = r < nv;
+      const uint8_t* src = v ? guq + static_cast<long long>(r0 + r) * 2 * f + cb * kTile + c * 16
+                             : guq;
+      cp_async_16z(smem_u32(in->g + r * kTile + c * 16), src, v);
+      cp_async_16z(smem_u32(in->u + r * kTile + c * 16), v ? src + f : guq, v);
     }
-    float cg[4], cu[4];
-    e4m3x4_decode(qg, cg);
-    e4m3x4_decode(qu, cu);
-    const float dhv[4] = {bf16_bits_to_f32(static_cast<uint16_t>(d2.x & 0xFFFFu)),
-                          bf16_bits_to_f32(static_cast<uint16_t>(d2.x >> 16)),
-                          bf16_bits_to_f32(static_cast<uint16_t>(d2.y & 0xFFFFu)),
-                          bf16_bits_to_f32(static_cast<uint16_t>(d2.y >> 16))};
-    float mg = 0.0f, mu = 0.0f;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const SwigluVals v = swiglu_bwd_at(cg[j], cu[j], sg, su, dhv[j]);
-      hv[i][j] = v.h;
-      gv[i][j] = v.dg;
-      uv[i][j] = v.du;
-      mg = fmaxf(mg, fabsf(v.dg));
-      mu = fmaxf(mu, fabsf(v.du));
-      cm[0][j] = fmaxf(cm[0][j], fabsf(v.h));
-      cm[1][j] = fmaxf(cm[1][j], fabsf(v.dg));
-      cm[2][j] = fmaxf(cm[2][j], fabsf(v.du));
+    for (int i = threadIdx.x; i < kTile * 16; i += kSwThreads) {     // dh: 16 x 16 B a row
+      const int r = i >> 4, c = i & 15;
+      const bool v = r < nv;
+      const uint16_t* src = v ? dh + static_cast<long long>(r0 + r) * f + cb * kTile + c * 8 : dh;
+      cp_async_16z(smem_u32(in->dh + r * kTile + c * 8), src, v);
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      mg = fmaxf(mg, __shfl_xor_sync(0xFFFFFFFFu, mg, off));
-      mu = fmaxf(mu, __shfl_xor_sync(0xFFFFFFFFu, mu, off));
+    if (threadIdx.x < 2 * kTile) {
+      const int r = threadIdx.x & (kTile - 1), which = threadIdx.x >> 7;
+      const bool v = r < nv;
+      const float* src = v ? sgu + static_cast<long long>(which ? NB + cb : cb) * R + r0 + r : sgu;
+      cp_async_4z(smem_u32((which ? in->su : in->sg) + r), src, v);
     }
-    const float s_g = e4m3_scale_from_amax(mg), s_u = e4m3_scale_from_amax(mu);
-    rs_g[i] = s_g;
-    rs_u[i] = s_u;
-    if (lane == 0 && r < nv) {
-      sdgu[static_cast<long long>(cb) * R + r0 + r] = s_g;
-      sdgu[static_cast<long long>(NB + cb) * R + r0 + r] = s_u;
-    }
+  };
+
+  int t = blockIdx.x;
+  if (t < ntiles) {
+    int rb, cb, r0, nv;
+    tile_of(t, rb, cb, r0, nv);
+    load_tile(buf, r0, nv, cb);
   }
+  cp_async_commit();
+  for (int i = 0; t < ntiles; t += gridDim.x, ++i) {
+    const int tn = t + static_cast<int>(gridDim.x);
+    if (tn < ntiles) {                          // the next tile's inputs, into the other buffer
+      int rb, cb, r0, nv;
+      tile_of(tn, rb, cb, r0, nv);
+      load_tile(buf + ((i + 1) & 1), r0, nv, cb);
+    }
+    cp_async_commit();                          // one group per iteration (possibly empty)
+    cp_async_wait<1>();                         // this tile's group has landed
+    __syncthreads();
+    const SwTile* in = buf + (i & 1);
+    int rb, cb, r0, nv;
+    tile_of(t, rb, cb, r0, nv);
+    const int c0 = cb * kTile + 4 * lane;         // this lane's first hidden column
+    float hv[8][4], gv[8][4], uv[8][4];           // h, dG, dU of the warp's 8 rows
+    float cm[3][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    float rs_g[8], rs_u[8];                       // the rows' 1x128 scales
 #pragma unroll
-  for (int t = 0; t < 3; ++t)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) cpart[warp][t][4 * lane + j] = cm[t][j];
-  __syncthreads();
-  if (threadIdx.x < 3 * kTile) {
-    const int t = threadIdx.x / kTile, c = threadIdx.x % kTile;
-    float m = 0.0f;
-#pragma unroll
-    for (int w = 0; w < 16; ++w) m = fmaxf(m, cpart[w][t][c]);
-    const float sc = pow2_scale_from_amax(m);
-    cscale[t][c] = sc;
-    float* dst = t == 0 ? shT + static_cast<long long>(blockIdx.x) * f
-                        : sdguT + static_cast<long long>(blockIdx.x) * 2 * f + (t - 1) * f;
-    dst[cb * kTile + c] = sc;
-  }
-  __syncthreads();
-  // row-major 1x128 codes of dG and dU (correctly rounded division, the quantiser's rule)
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int r = 8 * warp + i;
-    if (r < nv) {
-      uint32_t wg = 0, wu = 0;
+    for (int k = 0; k < 8; ++k) {
+      const int r = 8 * warp + k;
+      const uint32_t qg = *reinterpret_cast<const uint32_t*>(in->g + r * kTile + 4 * lane);
+      const uint32_t qu = *reinterpret_cast<const uint32_t*>(in->u + r * kTile + 4 * lane);
+      const uint2 d2 = *reinterpret_cast<const uint2*>(in->dh + r * kTile + 4 * lane);
+      const float sg = in->sg[r], su = in->su[r];
+      float cg[4], cu[4];
+      e4m3x4_decode(qg, cg);
+      e4m3x4_decode(qu, cu);
+      const float dhv[4] = {bf16_bits_to_f32(static_cast<uint16_t>(d2.x & 0xFFFFu)),
+                            bf16_bits_to_f32(static_cast<uint16_t>(d2.x >> 16)),
+                            bf16_bits_to_f32(static_cast<uint16_t>(d2.y & 0xFFFFu)),
+                            bf16_bits_to_f32(static_cast<uint16_t>(d2.y >> 16))};
+      float mg = 0.0f, mu = 0.0f;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        wg |= e4m3_byte(__fdiv_rn(gv[i][j], rs_g[i])) << (8 * j);
-        wu |= e4m3_byte(__fdiv_rn(uv[i][j], rs_u[i])) << (8 * j);
+        const SwigluVals v = swiglu_bwd_at(cg[j], cu[j], sg, su, dhv[j]);
+        hv[k][j] = v.h;
+        gv[k][j] = v.dg;
+        uv[k][j] = v.du;
+        mg = fmaxf(mg, fabsf(v.dg));
+        mu = fmaxf(mu, fabsf(v.du));
+        cm[0][j] = fmaxf(cm[0][j], fabsf(v.h));
+        cm[1][j] = fmaxf(cm[1][j], fabsf(v.dg));
+        cm[2][j] = fmaxf(cm[2][j], fabsf(v.du));
       }
-      uint8_t* out = dguq + static_cast<long long>(r0 + r) * 2 * f;
-      *reinterpret_cast<uint32_t*>(out + c0) = wg;
-      *reinterpret_cast<uint32_t*>(out + f + c0) = wu;
-    }
-  }
-  // transposed 128x1 codes: 8 rows (bytes) per column and thread; padded rows are 0
-  const long long p = static_cast<long long>(blockIdx.x) * kTile + 8 * warp;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int col = c0 + j;
-    const float rh = __frcp_rn(cscale[0][4 * lane + j]);    // exact: powers of two
-    const float rg = __frcp_rn(cscale[1][4 * lane + j]);
-    const float ru = __frcp_rn(cscale[2][4 * lane + j]);
-    uint32_t h0 = 0, h1 = 0, g0 = 0, g1 = 0, u0 = 0, u1 = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      h0 |= e4m3_byte(hv[i][j] * rh) << (8 * i);
-      h1 |= e4m3_byte(hv[i + 4][j] * rh) << (8 * i);
-      g0 |= e4m3_byte(gv[i][j] * rg) << (8 * i);
-      g1 |= e4m3_byte(gv[i + 4][j] * rg) << (8 * i);
-      u0 |= e4m3_byte(uv[i][j] * ru) << (8 * i);
-      u1 |= e4m3_byte(uv[i + 4][j] * ru) << (8 * i);
+      for (int off = 16; off > 0; off >>= 1) {
+        mg = fmaxf(mg, __shfl_xor_sync(0xFFFFFFFFu, mg, off));
+        mu = fmaxf(mu, __shfl_xor_sync(0xFFFFFFFFu, mu, off));
+      }
+      const float s_g = e4m3_scale_from_amax(mg), s_u = e4m3_scale_from_amax(mu);
+      rs_g[k] = s_g;
+      rs_u[k] = s_u;
+      if (lane == 0 && r < nv) {
+        sdgu[static_cast<long long>(cb) * R + r0 + r] = s_g;
+        sdgu[static_cast<long long>(NB + cb) * R + r0 + r] = s_u;
+      }
     }
-    *reinterpret_cast<uint2*>(hT + static_cast<long long>(col) * ldq + p) = make_uint2(h0, h1);
-    *reinterpret_cast<uint2*>(dguT + static_cast<long long>(col) * ldq + p) = make_uint2(g0, g1);
-    *reinterpret_cast<uint2*>(dguT + static_cast<long long>(f + col) * ldq + p) = make_uint2(u0, u1);
+#pragma unroll
+    for (int k = 0; k < 3; ++k)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) cpart[warp][k][4 * lane + j] = cm[k][j];
+    __syncthreads();
+    if (threadIdx.x < 3 * kTile) {
+      const int k = threadIdx.x / kTile, c = threadIdx.x % kTile;
+      float m = 0.0f;
+#pragma unroll
+      for (int w = 0; w < 16; ++w) m = fmaxf(m, cpart[w][k][c]);
+      const float sc = pow2_scale_from_amax(m);
+      cscale[k][c] = sc;
+      float* dst = k == 0 ? shT + static_cast<long long>(rb) * f
+                          : sdguT + static_cast<long long>(rb) * 2 * f + (k - 1) * f;
+      dst[cb * kTile + c] = sc;
+    }
+    __syncthreads();
+    // row-major 1x128 codes of dG and dU (correctly rounded division, the quantiser's rule)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int r = 8 * warp + k;
+      if (r < nv) {
+        uint32_t wg = 0, wu = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          wg |= e4m3_byte(__fdiv_rn(gv[k][j], rs_g[k])) << (8 * j);
+          wu |= e4m3_byte(__fdiv_rn(uv[k][j], rs_u[k])) << (8 * j);
+        }
+        uint8_t* out = dguq + static_cast<long long>(r0 + r) * 2 * f;
+        *reinterpret_cast<uint32_t*>(out + c0) = wg;
+        *reinterpret_cast<uint32_t*>(out + f + c0) = wu;
+      }
+    }
+    // transposed 128x1 codes: 8 rows (bytes) per column and thread; padded rows are 0
+    const long long pcol = static_cast<long long>(rb) * kTile + 8 * warp;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int col = c0 + j;
+      const float rh = __frcp_rn(cscale[0][4 * lane + j]);    // exact: powers of two
+      const float rg = __frcp_rn(cscale[1][4 * lane + j]);
+      const float ru = __frcp_rn(cscale[2][4 * lane + j]);
+      uint32_t h0 = 0, h1 = 0, g0 = 0, g1 = 0, u0 = 0, u1 = 0;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        h0 |= e4m3_byte(hv[k][j] * rh) << (8 * k);
+        h1 |= e4m3_byte(hv[k + 4][j] * rh) << (8 * k);
+        g0 |= e4m3_byte(gv[k][j] * rg) << (8 * k);
+        g1 |= e4m3_byte(gv[k + 4][j] * rg) << (8 * k);
+        u0 |= e4m3_byte(uv[k][j] * ru) << (8 * k);
+        u1 |= e4m3_byte(uv[k + 4][j] * ru) << (8 * k);
+      }
+      *reinterpret_cast<uint2*>(hT + static_cast<long long>(col) * ldq + pcol) = make_uint2(h0, h1);
+      *reinterpret_cast<uint2*>(dguT + static_cast<long long>(col) * ldq + pcol) = make_uint2(g0, g1);
+      *reinterpret_cast<uint2*>(dguT + static_cast<long long>(f + col) * ldq + pcol) =
+          make_uint2(u0, u1);
+    }
+    __syncthreads();                            // cscale and this input buffer are reused
   }
+  cp_async_wait<0>();
 }
 
 // ---- host launchers ------------------------------------------------------------------------
@@ -425,7 +502,14 @@ int launch_swiglu_bwd(const uint8_t* guq, const float* sgu, const uint16_t* dh, 
                       const int32_t* seg, const int32_t* pad, int G, int max_blocks, int ldq,
                       uint8_t* dguq, float* sdgu, uint8_t* hT, float* shT, uint8_t* dguT,
                       float* sdguT, cudaStream_t stream) {
-  swiglu_bwd_kernel<<<dim3(max_blocks, f / kTile), kSwThreads, 0, stream>>>(
+  if (set_max_dynamic_smem(reinterpret_cast<const void*>(swiglu_bwd_kernel), kSwSmem) != MOE_OK)
+    return MOE_ERR_CUDA;
+  // persistent: one block per SM (or per tile when there are fewer), tiles counted on the
+  // device from the padded offsets
+  long long grid = static_cast<long long>(max_blocks) * (f / kTile);
+  if (grid > num_sms()) grid = num_sms();
+  if (grid < 1) grid = 1;
+  swiglu_bwd_kernel<<<static_cast<unsigned>(grid), kSwThreads, kSwSmem, stream>>>(
       guq, sgu, dh, R, f, seg, pad, G, ldq, dguq, sdgu, hT, shT, dguT, sdguT);
   return check_launch();
 }

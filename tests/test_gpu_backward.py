@@ -125,11 +125,16 @@ def test_wgrad_reports_bad_pad_table():
         assert ops.status_value(st) == -6, bad
 
 
-def test_swiglu_bwd_against_oracle():
+@pytest.mark.parametrize("counts,f", [
+    ([130, 0, 77, 256, 1], 256),
+    # more tiles than SMs: each persistent block streams several tiles through its two
+    # shared-memory input buffers
+    ([1300, 0, 777, 2560, 1, 129], 1024),
+])
+def test_swiglu_bwd_against_oracle(counts, f):
     rng = np.random.default_rng(4)
-    counts = [130, 0, 77, 256, 1]
     seg = _seg(counts)
-    R, f, G = int(seg[-1]), 256, len(counts)
+    R, G = int(seg[-1]), len(counts)
     g = (rng.standard_normal((R, f)) * 3).astype(np.float32)
     u = rng.standard_normal((R, f)).astype(np.float32)
     gq, sg = oracle.quant_1x128(g)
