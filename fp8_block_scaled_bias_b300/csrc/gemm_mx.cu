@@ -85,10 +85,11 @@ struct Tile {
   static constexpr int OFF_USTART = OFF_SEG + (MAX_G + 1) * 4;
   static constexpr int OFF_WSUM = OFF_USTART + (MAX_G + 1) * 4;
   static constexpr int OFF_AMAX = OFF_WSUM + 32 * 4;         // [2 tiles][2 halves][128 rows]
-  // FP32 output: per epilogue warp a [32 rows][36] float staging tile for coalesced stores
-  static constexpr int STG_LD = 36;
-  static constexpr int OFF_STG = OFF_AMAX + 2 * 2 * 128 * 4;
-  static constexpr int SMEM_USED = OFF_STG + (F32OUT ? EPI_WARPS * 32 * STG_LD * 4 : 0);
+  // FP32 output: per epilogue warp two 4 KB boxes (32 rows x 32 floats, 128-byte swizzle)
+  // that TMA stores write out; 1024-byte aligned like the swizzle atom
+  static constexpr int STG_BOX = 32 * 32 * 4;
+  static constexpr int OFF_STG = (OFF_AMAX + 2 * 2 * 128 * 4 + 1023) & ~1023;
+  static constexpr int SMEM_USED = OFF_STG + (F32OUT ? EPI_WARPS * 2 * STG_BOX : 0);
   static constexpr int SMEM_ALLOC = SMEM_USED + 1024;
   static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 };
@@ -186,7 +187,8 @@ MOE_DEV void mbar_drain_mx(uint32_t bar, uint32_t parity) {
 template <int EPI, bool PAIR>
 __global__ void __launch_bounds__(mx::THREADS, 1)
     fp8_mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                       const __grid_constant__ CUtensorMap tmB, const MxParams p) {
+                       const __grid_constant__ CUtensorMap tmB,
+                       const __grid_constant__ CUtensorMap tmC, const MxParams p) {
   using namespace mx;
   using TL = Tile<PAIR, EPI == kEpiF32>;
   constexpr int BM = TL::BM, BN = TL::BN, STAGES = TL::STAGES;
@@ -278,10 +280,12 @@ __global__ void __launch_bounds__(mx::THREADS, 1)
   // unit -> (segment g, first row m0, valid rows rv, N tile nt, first K block kb0, K blocks)
   auto unit_info = [&](int unit, int& g, int& m0, int& rv, int& nt, int& kb0, int& nkb) {
     if (WG) {
+      // N tiles fastest: the CTAs running together write whole rows of dW between them
       g = unit / (MT * NT);
       const int r = unit - g * MT * NT;
-      nt = r / MT;
-      m0 = (r - nt * MT) * 128;
+      const int mt = r / NT;
+      nt = r - mt * NT;
+      m0 = mt * 128;
       rv = 128;
       kb0 = seg[g] / BK;
       nkb = (seg[g + 1] - seg[g]) / BK;
@@ -497,37 +501,38 @@ __global__ void __launch_bounds__(mx::THREADS, 1)
       const uint32_t tbase = tmem_base + lane_addr + static_cast<uint32_t>(grp * 128);
       if (WG) {
         // FP32 weight gradient: the warp's 32 rows x 128 columns of its half, 32 columns at
-        // a time through a shared-memory tile, so each store instruction writes four rows'
-        // 128 contiguous bytes (a row per lane would scatter 16 bytes over 32 rows)
+        // a time.  Each 32 x 32 box goes into shared memory (row `lane`, 16-byte chunk k at
+        // position k ^ (lane & 7): the 128-byte swizzle) and leaves by a TMA store, two boxes
+        // in flight per warp.  The accumulator is released as soon as it has been read, so
+        // the next tile's MMAs run while the stores drain.
         const bool store = nt * BN + grp * 128 < p.N;
-        float* stg = reinterpret_cast<float*>(smem + TL::OFF_STG) +
-                     (warp - EPI_WARP0) * 32 * TL::STG_LD;
-        float* c0 = p.Cf + (static_cast<long long>(g) * p.M + m0 + q * 32) * p.ldc + nt * BN +
-                    grp * 128 + (lane & 7) * 4;
+        const uint32_t stg = sbase + TL::OFF_STG + (warp - EPI_WARP0) * 2 * TL::STG_BOX;
+        uint8_t* stg_p = smem + TL::OFF_STG + (warp - EPI_WARP0) * 2 * TL::STG_BOX;
+        const int y = g * p.M + m0 + q * 32;
 #pragma unroll
         for (int c = 0; c < 8; c += 2) {
           uint32_t v[2][16];
           tmem_ld_32x32b_x16(tbase + c * 16, v[0]);
           tmem_ld_32x32b_x16(tbase + c * 16 + 16, v[1]);
-          tmem_ld_wait();
-          float4* srow = reinterpret_cast<float4*>(stg + lane * TL::STG_LD);
-#pragma unroll
-          for (int h = 0; h < 2; ++h)
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              srow[h * 4 + i] =
-                  make_float4(__uint_as_float(v[h][4 * i]), __uint_as_float(v[h][4 * i + 1]),
-                              __uint_as_float(v[h][4 * i + 2]), __uint_as_float(v[h][4 * i + 3]));
+          const int bx = (c >> 1) & 1;
+          if (lane == 0) bulk_wait_group_read<1>();   // this box's store of two rounds ago
           __syncwarp();
+          tmem_ld_wait();
           if (store) {
+            uint8_t* row_p = stg_p + bx * TL::STG_BOX + lane * 128;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const int r = 4 * j + (lane >> 3);
-              *reinterpret_cast<float4*>(c0 + static_cast<long long>(r) * p.ldc + c * 16) =
-                  *reinterpret_cast<const float4*>(stg + r * TL::STG_LD + (lane & 7) * 4);
+            for (int k = 0; k < 8; ++k) {
+              const uint32_t* w = &v[k >> 2][(k & 3) * 4];
+              *reinterpret_cast<uint4*>(row_p + ((k ^ (lane & 7)) * 16)) =
+                  make_uint4(w[0], w[1], w[2], w[3]);
             }
+            fence_proxy_async();                      // visible to the TMA engine
           }
           __syncwarp();
+          if (store && lane == 0) {
+            tma_store_2d(&tmC, stg + bx * TL::STG_BOX, nt * BN + grp * 128 + c * 16, y);
+            bulk_commit_group();
+          }
         }
       } else if (PAIR) {
         // sub-tile grp (rows 128 grp + row of the block), all BN columns of its accumulator
@@ -634,6 +639,7 @@ __global__ void __launch_bounds__(mx::THREADS, 1)
       if (lane == 0) mbar_arrive(tempty_bar);
       ++tt;
     }
+    if (WG && lane == 0) bulk_wait_group<0>();     // every store complete before exit
   }
 
   tc_fence_before();
@@ -662,6 +668,12 @@ int launch_mx_kernel(const uint8_t* A, const uint8_t* B, const MxParams& p, cuda
   if (!encode_tmap_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, p.K,
                       static_cast<uint64_t>(WG ? 1 : p.G) * p.N, p.K, mx::BK, TL::BN))
     return MOE_ERR_CUDA;
+  // Wgrad: C is FP32 [G][M][ldc], written in 32 x 32 boxes; otherwise unused (a copy of A's)
+  CUtensorMap tmC = tmA;
+  if (WG && !encode_tmap_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.Cf, p.ldc,
+                            static_cast<uint64_t>(p.G) * p.M, static_cast<uint64_t>(p.ldc) * 4,
+                            32, 32))
+    return MOE_ERR_CUDA;
   if (set_max_dynamic_smem(reinterpret_cast<const void*>(fp8_mx_gemm_kernel<EPI, PAIR>),
                            TL::SMEM_ALLOC) != MOE_OK)
     return MOE_ERR_CUDA;
@@ -672,7 +684,7 @@ int launch_mx_kernel(const uint8_t* A, const uint8_t* B, const MxParams& p, cuda
   if (units < grid) grid = units;
   if (grid < 1) grid = 1;
   fp8_mx_gemm_kernel<EPI, PAIR>
-      <<<static_cast<unsigned>(grid), mx::THREADS, TL::SMEM_ALLOC, stream>>>(tmA, tmB, p);
+      <<<static_cast<unsigned>(grid), mx::THREADS, TL::SMEM_ALLOC, stream>>>(tmA, tmB, tmC, p);
   return check_launch();
 }
 }  // namespace
