@@ -145,6 +145,26 @@ MOE_DEV void tmem_st_x8(uint32_t taddr, const uint32_t (&r)[8]) {
 
 MOE_DEV void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// 2-D tiled store of one shared-memory box (bulk async-group completion); x, y >= 0.
+MOE_DEV void tma_store_2d(const void* tmap, uint32_t src, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(x), "r"(y), "r"(src)
+               : "memory");
+}
+
+MOE_DEV void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Wait until at most N of this thread's bulk groups still read their shared-memory source.
+template <int N>
+MOE_DEV void bulk_wait_group_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// Wait until at most N of this thread's bulk groups are still in flight.
+template <int N>
+MOE_DEV void bulk_wait_group() { asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory"); }
+
 
 // A power-of-two FP32 scale as a UE8M0 byte repeated four times (one per 32-deep step).
 // Anything else (zero, subnormal, inf/NaN, a mantissa bit set) is a data error.
