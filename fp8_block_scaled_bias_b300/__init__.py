@@ -7,7 +7,8 @@ point for torch tensors, ``layer`` chains them into one layer forward.
 
 from ._lib import LIB_PATH, MoEError, SIGNATURES, load
 from . import ops
-from .layer import MoELayer, MoEWeights, make_weights, interleave_gate_up, quantise_expert
+from .layer import (MoELayer, MoEWeights, make_weights, interleave_gate_up, quantise_expert,
+                    save_bias, load_bias)
 
 __all__ = ["LIB_PATH", "MoEError", "SIGNATURES", "load", "ops", "MoELayer", "MoEWeights",
-           "make_weights", "interleave_gate_up", "quantise_expert"]
+           "make_weights", "interleave_gate_up", "quantise_expert", "save_bias", "load_bias"]

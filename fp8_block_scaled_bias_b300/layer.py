@@ -41,6 +41,27 @@ class MoEWeights:
     s2: torch.Tensor          # FP32 [E+1, d/128, f/128]
 
 
+def save_bias(bias, path):
+    """Write the selection bias b [E] (FP32), the layer's only state that training
+    updates step by step ("DeepSeek-V3" summary, core idea 2), to a ``.npy`` file."""
+    import numpy as np
+    if bias.dtype != torch.float32 or bias.dim() != 1:
+        raise ValueError("bias must be a 1-D float32 tensor")
+    np.save(path, bias.detach().cpu().numpy())
+
+
+def load_bias(path, out):
+    """Read a bias saved by ``save_bias`` into ``out`` (a float32 [E] tensor on any device,
+    e.g. ``weights.bias``) in place; the stored length must equal E."""
+    import numpy as np
+    b = np.load(path)
+    if b.dtype != np.float32 or b.shape != tuple(out.shape) or out.dtype != torch.float32:
+        raise ValueError(f"stored bias {b.dtype}{list(b.shape)} does not fit "
+                         f"{out.dtype}{list(out.shape)}")
+    out.copy_(torch.from_numpy(b))
+    return out
+
+
 def interleave_gate_up(q1, s1, q3, s3):
     """Gate [f, d] and up [f, d] codes/scales -> the layout the gate/up GEMM takes.
 
